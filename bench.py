@@ -1,0 +1,414 @@
+#!/usr/bin/env python3
+"""Benchmark of the chunkwise KDA forward on GB300.
+
+Metric: KDA prefill tokens/s and µs per call on the 1 x 16384-token, H = 12
+prefill (K = V = 128, bf16 q/k/v, fp32 raw gate/beta, lower_bound -5, fp32
+paged pool), plus the fraction of the roofline.
+
+One "step" is one full forward (prep + intra-chunk + scan with the output and
+paged state I/O) over the whole workload.  Inputs are synthetic
+(kda_prefill_gb300.workloads) and resident in HBM before timing starts; the
+activations (about 252 MB per step) exceed the 126 MB L2, so no flush is
+needed between steps.
+
+Run:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+With N > 1 it is launched by torch.distributed.run, one rank per GPU; each rank
+runs an independent replica of the workload (the op has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s & µs/call (1×16K, H=12) and % of roofline on 1 GB300"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+# Algorithmic bytes per token-head: q, k, v (bf16, 256 B each), raw gate
+# (fp32, 512 B), raw beta (4 B) read, and out (bf16, 256 B) written.
+BYTES_PER_TOKHEAD = 1540
+INTRA_BYTES_PER_TOKHEAD = 1284   # what the chunk-parallel kernel must read
+SCAN_BYTES_PER_TOKHEAD = 256     # what the scan must write (+ state bytes)
+# Algorithmic FLOPs per token-head at the reference chunk of 64:
+# 2 * (5 C^2 d + 3 C d^2) / C with d = 128.
+FLOP_PER_TOKHEAD = 2 * (5 * 64 * 64 * 128 + 3 * 64 * 128 * 128) // 64
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="prefill_16k")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--clock-seconds", type=float, default=1.5,
+                    help="minimum span of the nvidia-smi clock sampling")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get(
+            "bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def state_bytes(w):
+    import torch
+    elt = torch.tensor([], dtype=w.state_pool.dtype).element_size()
+    plane = w.num_heads * 128 * 128 * elt
+    reads = int(w.has_initial_state.sum())
+    return plane * reads + plane * w.num_seqs
+
+
+# ---------------------------------------------------------------------------
+# nvidia-smi clock sampling
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="kda_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                if self.uuid and parts[1] != self.uuid:
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# Our implementation
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world):
+    import torch
+    import kda_prefill_gb300 as kda
+    from kda_prefill_gb300 import workloads as wl
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    kda.load_library()
+
+    w = wl.WORKLOADS[args.workload]()
+    T, H, N = w.total_tokens, w.num_heads, w.num_seqs
+    q, k, v = w.q.to(dev), w.k.to(dev), w.v.to(dev)
+    g, b = w.g_raw.to(dev), w.beta_raw.to(dev)
+    cu = w.cu_seqlens.to(dev)
+    storage = w.pool_storage.to(dev)
+    S, stride0 = storage.shape
+    pool = storage.as_strided((S, H, 128, 128), (stride0, 128 * 128, 128, 1))
+    idx, hs = w.state_indices.to(dev), w.has_initial_state.to(dev)
+    out = torch.empty_like(v)
+    ws = torch.empty(max(kda.workspace_size(T, N, H), 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.chunk_fwd(q, k, v, g, b, cu, state_cache=pool, state_indices=idx,
+                      has_initial_state=hs, out=out, lower_bound=w.lower_bound,
+                      cu_seqlens_cpu=w.cu_seqlens, workspace=ws)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+
+    uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None else None)
+    sampler.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    ms_total = e0.elapsed_time(e1)
+    # keep the GPU busy with the same step until the clock sampling spans
+    # enough samples (the timed region itself can be shorter than the
+    # sampling period)
+    t_end = sampler.t0 + args.clock_seconds
+    while time.time() < t_end:
+        step()
+        torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    ms_total = max_over_ranks(ms_total)
+    ms_step = ms_total / args.steps
+
+    # per-kernel times over a second timed region of K steps
+    kda.set_kernel_timing(True)
+    kda.kernel_times()
+    barrier()
+    for _ in range(args.steps):
+        step()
+    barrier()
+    ktimes, kcalls = kda.kernel_times()
+    kda.set_kernel_timing(False)
+    kavg = {n: t / max(kcalls, 1) for n, t in ktimes.items()}
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = {n: getattr(w, n).pin_memory() for n in ("q", "k", "v", "g_raw", "beta_raw")}
+        cu_h = w.cu_seqlens.pin_memory()
+        idx_h = w.state_indices.pin_memory()
+        hs_h = w.has_initial_state.pin_memory()
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in pin.values()) + \
+            sum(t.numel() * t.element_size() for t in (cu_h, idx_h, hs_h))
+        d2h = out_h.numel() * out_h.element_size()
+
+        def e2e_step():
+            q.copy_(pin["q"], non_blocking=True)
+            k.copy_(pin["k"], non_blocking=True)
+            v.copy_(pin["v"], non_blocking=True)
+            g.copy_(pin["g_raw"], non_blocking=True)
+            b.copy_(pin["beta_raw"], non_blocking=True)
+            cu.copy_(cu_h, non_blocking=True)
+            idx.copy_(idx_h, non_blocking=True)
+            hs.copy_(hs_h, non_blocking=True)
+            step()
+            out_h.copy_(out, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        barrier()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        a1.record(stream)
+        barrier()
+        e2e_ms = max_over_ranks(a0.elapsed_time(a1)) / args.steps
+        e2e = {"value": T * world / (e2e_ms / 1e3), "unit": UNIT,
+               "us_per_call": e2e_ms * 1e3,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    hbm, tf_burst, tf_sust, src = peaks()
+    bytes_alg = BYTES_PER_TOKHEAD * T * H + state_bytes(w)
+    flops_alg = FLOP_PER_TOKHEAD * T * H
+    t_roof = max(bytes_alg / (hbm * 1e9), flops_alg / (tf_burst * 1e12))
+    dom = max(kavg, key=kavg.get)
+    dom_bytes = (INTRA_BYTES_PER_TOKHEAD * T * H if dom == "kda_intra"
+                 else SCAN_BYTES_PER_TOKHEAD * T * H + state_bytes(w))
+    dom_gbs = dom_bytes / (kavg[dom] / 1e3) / 1e9
+    traffic = load_traffic(dom, args.workload)
+
+    n_launch_per_step = sum(1 for t in kavg.values() if t > 0)
+    line = {
+        "metric": METRIC,
+        "value": T * world / (ms_step / 1e3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "us_per_call": ms_step * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 inputs, fp32 accumulation",
+        "data": "synthetic (seeded, kda_prefill_gb300.workloads)",
+        "config": {"workload": w.name, "total_tokens": T, "num_seqs": N, "heads": H,
+                   "head_dim": 128, "lower_bound": w.lower_bound,
+                   "state_pool": f"{str(w.state_pool.dtype).replace('torch.', '')} "
+                                 f"[{S},{H},128,128]",
+                   "l2": "inputs exceed L2 (activations ~252 MB per step > 126 MB)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": dom_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": dom_gbs / hbm, "traffic": traffic, "kernel": dom,
+                     "kernel_us": kavg[dom] * 1e3, "peak_source": src},
+        "step_roofline": {"bytes_alg": bytes_alg, "flops_alg": flops_alg,
+                          "roofline_us": t_roof * 1e6, "frac": t_roof / (ms_step / 1e3),
+                          "achieved_gbs": bytes_alg / (ms_step / 1e3) / 1e9,
+                          "peak_gbs": hbm, "peak_source": src},
+        "kernels_us": {n: t * 1e3 for n, t in kavg.items()},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": n_launch_per_step * args.steps,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def load_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if the
+    kernel source has not changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d[kernel]
+        src = os.path.join(ROOT, "kda_prefill_gb300", "csrc", "kda_kernels.cu")
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if ent.get("source_sha") != sha or ent.get("workload") != workload:
+            return None
+        return ent["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline / reference arm
+# ---------------------------------------------------------------------------
+
+def _oracle_sample(w, heads):
+    import numpy as np
+    import oracle
+    hsel = list(heads)
+    q = w.q[0][:, hsel].double().numpy()
+    k = w.k[0][:, hsel].double().numpy()
+    v = w.v[0][:, hsel].double().numpy()
+    g = w.g_raw[0][:, hsel].double().numpy()
+    b = w.beta_raw[0][:, hsel].double().numpy()
+    N = w.num_seqs
+    flags = w.has_initial_state.numpy().astype(np.uint8)
+    init = np.zeros((N, len(hsel), 128, 128))
+    for n in range(N):
+        if flags[n]:
+            init[n] = w.state_pool[int(w.state_indices[n])][hsel].double().numpy()
+    cu = w.cu_seqlens.numpy()
+    t0 = time.perf_counter()
+    oracle.forward(q, k, v, g, b, cu, init, flags, lower_bound=w.lower_bound)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, heads=(0, 1, 2, 3)):
+    import oracle
+    oracle.load()
+    secs = _oracle_sample(w, heads)
+    frac = len(heads) / w.num_heads
+    return {"value": w.total_tokens * frac / secs, "unit": UNIT,
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "seconds": secs,
+            "sample": f"all {w.total_tokens} tokens of heads {list(heads)} of {w.num_heads} "
+                      f"(value scaled to the whole workload)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from kda_prefill_gb300 import workloads as wl
+    import oracle
+    oracle.load()
+    w = wl.WORKLOADS[args.workload]()
+    heads = (0,)
+    for _ in range(args.warmup):
+        _oracle_sample(w, heads)
+    secs = [_oracle_sample(w, heads) for _ in range(args.steps)]
+    per_step = sum(secs) / len(secs)
+    frac = len(heads) / w.num_heads
+    value = w.total_tokens * frac / per_step
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3 / frac,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded, kda_prefill_gb300.workloads)",
+        "config": {"workload": w.name, "total_tokens": w.total_tokens,
+                   "num_seqs": w.num_seqs, "heads": w.num_heads, "head_dim": 128},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"each step: all {w.total_tokens} tokens of head 0 of "
+                                   f"{w.num_heads} (value scaled to the whole workload)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world)
+
+
+if __name__ == "__main__":
+    main()

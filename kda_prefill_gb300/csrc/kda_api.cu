@@ -1,0 +1,696 @@
+// Host side of the C ABI declared in include/kda.h: argument validation, the
+// per-bounds metadata cache with its single pinned non-blocking upload, and
+// the kernel launches.
+//
+// Metadata (ROCm/aiter PR #6912, "Changes"): chunk indices are built from
+// host bounds and numbered by the sequence's position in cu_seqlens; all
+// tables share one int32 buffer whose blocks start 16-byte aligned, uploaded
+// with one non-blocking copy from pinned memory and cached on the bounds'
+// contents.  A hit from another stream waits on the uploading stream; a miss
+// while the stream is being captured fails; entries a capture used are kept for
+// the life of the process so eviction cannot free them under a graph.
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <list>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "kda.h"
+#include "kda_internal.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(KDA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kChunk = kda::kC;
+constexpr int kD = kda::kD;
+
+inline int64_t chunks_of(int64_t len) { return (len + kChunk - 1) / kChunk; }
+
+int64_t max_chunks(int64_t T, int32_t N) { return (T + kChunk - 1) / kChunk + N; }
+
+size_t state_elt(int dtype) { return dtype == KDA_STATE_F32 ? 4 : 2; }
+
+struct Range {
+    const char* name;
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+bool overlaps(const Range& a, const Range& b) {
+    if (a.lo == a.hi || b.lo == b.hi) return false;
+    return a.lo < b.hi && b.lo < a.hi;
+}
+
+Range rng(const char* name, const void* p, size_t bytes) {
+    uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Range{name, lo, p ? lo + bytes : lo};
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_host_bounds(const int32_t* cu, int32_t N, int64_t T) {
+    if (cu[0] != 0) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens_host[0] = %d, expected 0", cu[0]);
+    for (int32_t n = 0; n < N; ++n)
+        if (cu[n + 1] < cu[n])
+            return fail(KDA_ERR_INVALID_ARG, "cu_seqlens_host decreases at %d (%d -> %d)", n,
+                        cu[n], cu[n + 1]);
+    if ((int64_t)cu[N] != T)
+        return fail(KDA_ERR_INVALID_ARG, "cu_seqlens_host[%d] = %d, expected total_tokens = %lld",
+                    N, cu[N], (long long)T);
+    return KDA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Metadata: layout of the single int32 buffer.
+// ---------------------------------------------------------------------------
+struct MetaLayout {
+    int64_t n_chunks = 0;
+    size_t off_cu = 0, off_seq_off = 0, off_chunk_seq = 0, off_chunk_tok = 0;  // int32 units
+    size_t words = 0;
+};
+
+inline size_t align4(size_t w) { return (w + 3) & ~size_t(3); }  // 16-byte blocks
+
+MetaLayout meta_layout(int32_t N, int64_t n_chunks) {
+    MetaLayout L;
+    L.n_chunks = n_chunks;
+    size_t o = 0;
+    L.off_cu = o;        o = align4(o + (size_t)N + 1);
+    L.off_seq_off = o;   o = align4(o + (size_t)N + 1);
+    L.off_chunk_seq = o; o = align4(o + (size_t)n_chunks);
+    L.off_chunk_tok = o; o = align4(o + (size_t)n_chunks);
+    L.words = std::max<size_t>(o, 4);
+    return L;
+}
+
+void meta_fill(const int32_t* cu, int32_t N, const MetaLayout& L, int32_t* buf) {
+    std::memset(buf, 0, L.words * sizeof(int32_t));
+    int32_t* mcu = buf + L.off_cu;
+    int32_t* off = buf + L.off_seq_off;
+    int32_t* cseq = buf + L.off_chunk_seq;
+    int32_t* ctok = buf + L.off_chunk_tok;
+    int64_t j = 0;
+    for (int32_t n = 0; n < N; ++n) {
+        mcu[n] = cu[n];
+        off[n] = (int32_t)j;
+        const int64_t nc = chunks_of((int64_t)cu[n + 1] - cu[n]);
+        for (int64_t c = 0; c < nc; ++c, ++j) {
+            cseq[j] = n;
+            ctok[j] = (int32_t)(cu[n] + c * kChunk);
+        }
+    }
+    mcu[N] = cu[N];
+    off[N] = (int32_t)j;
+}
+
+// ---------------------------------------------------------------------------
+// Pinned staging ring for uploads and the read-back.  Allocated once per
+// process; a region is reused only after the copy that last used it has
+// completed.
+// ---------------------------------------------------------------------------
+class PinnedRing {
+  public:
+    static constexpr size_t kBytes = size_t(8) << 20;
+
+    // Returns a staging area of `bytes` (16-aligned) or nullptr on failure.
+    // The caller records `*done` after enqueueing its copy.
+    void* acquire(size_t bytes, cudaEvent_t** done, bool* owned_separately) {
+        bytes = (bytes + 255) & ~size_t(255);
+        *owned_separately = false;
+        if (bytes > kBytes) {
+            void* p = nullptr;
+            if (cudaHostAlloc(&p, bytes, cudaHostAllocDefault) != cudaSuccess) return nullptr;
+            *owned_separately = true;
+            *done = nullptr;
+            return p;
+        }
+        if (!base_) {
+            if (cudaHostAlloc(&base_, kBytes, cudaHostAllocDefault) != cudaSuccess) {
+                base_ = nullptr;
+                return nullptr;
+            }
+        }
+        if (head_ + bytes > kBytes) head_ = 0;
+        const size_t lo = head_, hi = head_ + bytes;
+        // wait for (and drop) earlier copies that used this region
+        for (auto it = pending_.begin(); it != pending_.end();) {
+            if (it->lo < hi && lo < it->hi) {
+                cudaEventSynchronize(it->ev);
+                cudaEventDestroy(it->ev);
+                it = pending_.erase(it);
+            } else {
+                ++it;
+            }
+        }
+        pending_.push_back(Pending{lo, hi, nullptr});
+        cudaEventCreateWithFlags(&pending_.back().ev, cudaEventDisableTiming);
+        *done = &pending_.back().ev;
+        head_ = hi;
+        return static_cast<char*>(base_) + lo;
+    }
+
+  private:
+    struct Pending {
+        size_t lo, hi;
+        cudaEvent_t ev;
+    };
+    void* base_ = nullptr;
+    size_t head_ = 0;
+    std::list<Pending> pending_;
+};
+
+struct MetaEntry {
+    std::vector<int32_t> key;  // device, N, bounds
+    int device = 0;
+    MetaLayout layout;
+    int32_t* dev = nullptr;
+    void* host_own = nullptr;  // pinned buffer owned by this entry (large metadata only)
+    cudaEvent_t ready = nullptr;
+    cudaStream_t upload_stream = nullptr;
+    bool captured = false;
+    std::vector<std::pair<cudaStream_t, cudaEvent_t>> uses;  // last use per stream
+    uint64_t stamp = 0;
+};
+
+class MetaCache {
+  public:
+    static constexpr size_t kMaxEntries = 256;
+
+    std::mutex mu;
+    std::map<std::vector<int32_t>, MetaEntry*> map;
+    PinnedRing ring;
+    uint64_t clock = 0;
+
+    // Finds or builds the entry for these bounds; enqueues the upload on a miss
+    // and the cross-stream wait on a hit.
+    int get(const int32_t* cu, int32_t N, cudaStream_t stream, bool capturing, MetaEntry** out) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+        std::vector<int32_t> key;
+        key.reserve((size_t)N + 3);
+        key.push_back(dev);
+        key.push_back(kChunk);
+        key.push_back(N);
+        key.insert(key.end(), cu, cu + N + 1);
+        auto it = map.find(key);
+        if (it != map.end()) {
+            MetaEntry* m = it->second;
+            m->stamp = ++clock;
+            if (m->upload_stream != stream) {
+                cudaError_t q = cudaEventQuery(m->ready);
+                if (q == cudaErrorNotReady) {
+                    if (capturing)
+                        return fail(KDA_ERR_CAPTURE_MISS,
+                                    "metadata upload still in flight on another stream while "
+                                    "this stream is capturing; synchronize before capturing");
+                    e = cudaStreamWaitEvent(stream, m->ready, 0);
+                    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
+                } else if (q != cudaSuccess) {
+                    return cuda_fail(q, "cudaEventQuery");
+                }
+            }
+            if (capturing) m->captured = true;
+            *out = m;
+            return KDA_OK;
+        }
+        if (capturing)
+            return fail(KDA_ERR_CAPTURE_MISS,
+                        "metadata for these bounds is not cached and the stream is capturing; "
+                        "run the call once before capture");
+        int rc = evict_if_full(stream);
+        if (rc != KDA_OK) return rc;
+
+        int64_t n_chunks = 0;
+        for (int32_t n = 0; n < N; ++n) n_chunks += chunks_of((int64_t)cu[n + 1] - cu[n]);
+        auto* m = new MetaEntry();
+        m->key = std::move(key);
+        m->device = dev;
+        m->layout = meta_layout(N, n_chunks);
+        const size_t bytes = m->layout.words * sizeof(int32_t);
+        cudaEvent_t* done = nullptr;
+        bool separate = false;
+        void* host = ring.acquire(bytes, &done, &separate);
+        if (!host) {
+            delete m;
+            return fail(KDA_ERR_CUDA, "pinned staging allocation failed");
+        }
+        if (separate) m->host_own = host;
+        meta_fill(cu, N, m->layout, static_cast<int32_t*>(host));
+        e = cudaMallocAsync(reinterpret_cast<void**>(&m->dev), bytes, stream);
+        if (e != cudaSuccess) {
+            if (m->host_own) cudaFreeHost(m->host_own);
+            delete m;
+            return cuda_fail(e, "cudaMallocAsync (metadata)");
+        }
+        e = cudaMemcpyAsync(m->dev, host, bytes, cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (metadata upload)");
+        if (done) cudaEventRecord(*done, stream);
+        cudaEventCreateWithFlags(&m->ready, cudaEventDisableTiming);
+        cudaEventRecord(m->ready, stream);
+        m->upload_stream = stream;
+        m->stamp = ++clock;
+        map[m->key] = m;
+        *out = m;
+        return KDA_OK;
+    }
+
+    // Records that `stream` used the entry (for safe eviction later).
+    void mark_use(MetaEntry* m, cudaStream_t stream, bool capturing) {
+        if (capturing) return;
+        for (auto& u : m->uses) {
+            if (u.first == stream) {
+                cudaEventRecord(u.second, stream);
+                return;
+            }
+        }
+        cudaEvent_t ev;
+        if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return;
+        cudaEventRecord(ev, stream);
+        m->uses.emplace_back(stream, ev);
+    }
+
+    int evict_if_full(cudaStream_t stream) {
+        while (map.size() >= kMaxEntries) {
+            auto victim = map.end();
+            for (auto it = map.begin(); it != map.end(); ++it) {
+                if (it->second->captured) continue;
+                if (victim == map.end() || it->second->stamp < victim->second->stamp) victim = it;
+            }
+            if (victim == map.end()) return KDA_OK;  // everything captured: keep growing
+            MetaEntry* m = victim->second;
+            int dev = 0;
+            cudaGetDevice(&dev);
+            if (m->device == dev) {
+                // free stream-ordered after every recorded use
+                for (auto& u : m->uses) cudaStreamWaitEvent(stream, u.second, 0);
+                cudaStreamWaitEvent(stream, m->ready, 0);
+                cudaFreeAsync(m->dev, stream);
+            } else {
+                leaked_.push_back(m->dev);  // other device: released by kda_release_cache
+            }
+            destroy_events(m);
+            if (m->host_own) leaked_host_.push_back(m->host_own);
+            map.erase(victim);
+            delete m;
+        }
+        return KDA_OK;
+    }
+
+    static void destroy_events(MetaEntry* m) {
+        for (auto& u : m->uses) cudaEventDestroy(u.second);
+        m->uses.clear();
+        if (m->ready) cudaEventDestroy(m->ready);
+        m->ready = nullptr;
+    }
+
+    int release() {
+        int rc = KDA_OK;
+        int cur = 0;
+        cudaGetDevice(&cur);
+        for (auto it = map.begin(); it != map.end();) {
+            MetaEntry* m = it->second;
+            if (m->captured) {
+                ++it;
+                continue;
+            }
+            cudaSetDevice(m->device);
+            if (cudaDeviceSynchronize() != cudaSuccess) rc = KDA_ERR_CUDA;
+            cudaFree(m->dev);
+            if (m->host_own) cudaFreeHost(m->host_own);
+            destroy_events(m);
+            delete m;
+            it = map.erase(it);
+        }
+        for (void* p : leaked_) cudaFree(p);
+        leaked_.clear();
+        for (void* p : leaked_host_) cudaFreeHost(p);
+        leaked_host_.clear();
+        cudaSetDevice(cur);
+        return rc;
+    }
+
+  private:
+    std::vector<void*> leaked_;
+    std::vector<void*> leaked_host_;
+};
+
+MetaCache& cache() {
+    static MetaCache* c = new MetaCache();  // never destroyed: outlives static teardown
+    return *c;
+}
+
+// Per-kernel timing records (guarded by the cache mutex).
+struct Timing {
+    bool enabled = false;
+    std::vector<std::vector<cudaEvent_t>> calls;  // kNumKernels + 1 marks per call
+    std::vector<cudaEvent_t> free_events;
+
+    cudaEvent_t take() {
+        if (!free_events.empty()) {
+            cudaEvent_t e = free_events.back();
+            free_events.pop_back();
+            return e;
+        }
+        cudaEvent_t e = nullptr;
+        cudaEventCreate(&e);
+        return e;
+    }
+};
+
+Timing& timing() {
+    static Timing* t = new Timing();
+    return *t;
+}
+
+struct StateArgs {
+    const void* in;
+    void* out;
+    int64_t in_stride, out_stride;
+    const int32_t* in_idx;
+    const int32_t* out_idx;
+    const uint8_t* has_init;
+};
+
+int run_forward(const void* q, const void* k, const void* v, const float* g_raw,
+                const float* beta_raw, const int32_t* cu_dev, const int32_t* cu_host,
+                int32_t N, int64_t T, int32_t H, const StateArgs& st, int state_dtype,
+                void* out, float lower_bound, void* workspace, size_t workspace_bytes,
+                cudaStream_t stream) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    const bool capturing = (cap != cudaStreamCaptureStatusNone);
+
+    std::lock_guard<std::mutex> lock(cache().mu);
+    std::vector<int32_t> readback;
+    if (!cu_host) {
+        if (capturing)
+            return fail(KDA_ERR_CAPTURE_MISS,
+                        "device bounds cannot be read back while the stream is capturing; "
+                        "pass cu_seqlens_host");
+        readback.resize((size_t)N + 1);
+        cudaEvent_t* done = nullptr;
+        bool separate = false;
+        void* host = cache().ring.acquire(readback.size() * sizeof(int32_t), &done, &separate);
+        if (!host) return fail(KDA_ERR_CUDA, "pinned staging allocation failed");
+        e = cudaMemcpyAsync(host, cu_dev, readback.size() * sizeof(int32_t),
+                            cudaMemcpyDeviceToHost, stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+        if (e == cudaSuccess) std::memcpy(readback.data(), host, readback.size() * sizeof(int32_t));
+        if (done) cudaEventRecord(*done, stream);
+        if (separate) cudaFreeHost(host);
+        if (e != cudaSuccess) return cuda_fail(e, "read-back of cu_seqlens");
+        cu_host = readback.data();
+        int rc = check_host_bounds(cu_host, N, T);
+        if (rc != KDA_OK) return rc;
+    }
+
+    MetaEntry* m = nullptr;
+    int rc = cache().get(cu_host, N, stream, capturing, &m);
+    if (rc != KDA_OK) return rc;
+
+    const int64_t bound = max_chunks(T, N);
+    const kda::WsLayout L = kda::workspace_layout(bound, H);
+    char* ws = static_cast<char*>(workspace);
+
+    kda::FwdParams p{};
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k = static_cast<const __nv_bfloat16*>(k);
+    p.v = static_cast<const __nv_bfloat16*>(v);
+    p.g_raw = g_raw;
+    p.beta_raw = beta_raw;
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.H = H;
+    p.N = N;
+    p.n_chunks = (int)m->layout.n_chunks;
+    p.T = T;
+    p.lower_bound = lower_bound;
+    p.cu = m->dev + m->layout.off_cu;
+    p.seq_off = m->dev + m->layout.off_seq_off;
+    p.chunk_seq = m->dev + m->layout.off_chunk_seq;
+    p.chunk_tok = m->dev + m->layout.off_chunk_tok;
+    p.ws_w = reinterpret_cast<float*>(ws + L.off_w);
+    p.ws_qg = reinterpret_cast<float*>(ws + L.off_qg);
+    p.ws_kg = reinterpret_cast<float*>(ws + L.off_kg);
+    p.ws_u = reinterpret_cast<float*>(ws + L.off_u);
+    p.ws_aqk = reinterpret_cast<float*>(ws + L.off_aqk);
+    p.ws_gamma = reinterpret_cast<float*>(ws + L.off_gamma);
+    p.st_in = st.in;
+    p.st_out = st.out;
+    p.st_in_stride = st.in_stride;
+    p.st_out_stride = st.out_stride;
+    p.st_in_idx = st.in_idx;
+    p.st_out_idx = st.out_idx;
+    p.has_init = st.has_init;
+    p.st_dtype = state_dtype;
+    (void)workspace_bytes;
+
+    cudaEvent_t* marks = nullptr;
+    std::vector<cudaEvent_t> ev;
+    if (timing().enabled && !capturing) {
+        for (int i = 0; i <= kda::kNumKernels; ++i) ev.push_back(timing().take());
+        marks = ev.data();
+    }
+    e = kda::launch_forward(p, stream, marks);
+    if (marks) timing().calls.push_back(ev);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    cache().mark_use(m, stream, capturing);
+    return KDA_OK;
+}
+
+int common_checks(const void* q, const void* k, const void* v, const float* g_raw,
+                  const float* beta_raw, const int32_t* cu_dev, const int32_t* cu_host,
+                  int32_t N, int64_t T, int32_t H, void* out, float lower_bound,
+                  int state_dtype, void* workspace, size_t workspace_bytes) {
+    if (N < 0) return fail(KDA_ERR_INVALID_ARG, "num_seqs = %d < 0", N);
+    if (T < 0) return fail(KDA_ERR_INVALID_ARG, "total_tokens = %lld < 0", (long long)T);
+    if (T > INT32_MAX - kChunk)
+        return fail(KDA_ERR_INVALID_ARG, "total_tokens = %lld exceeds the int32 token index",
+                    (long long)T);
+    if (H <= 0 || H > 65535) return fail(KDA_ERR_INVALID_ARG, "num_heads = %d out of range", H);
+    if (N == 0 && T != 0) return fail(KDA_ERR_INVALID_ARG, "tokens without sequences");
+    if (state_dtype < KDA_STATE_F32 || state_dtype > KDA_STATE_F16)
+        return fail(KDA_ERR_UNSUPPORTED, "state_dtype %d not supported (0 fp32, 1 bf16, 2 fp16)",
+                    state_dtype);
+    if (!(lower_bound <= 0.0f && lower_bound >= -64.0f))
+        return fail(KDA_ERR_UNSUPPORTED, "lower_bound %g outside [-64, 0]", (double)lower_bound);
+    if (!cu_dev && !cu_host)
+        return fail(KDA_ERR_INVALID_ARG, "cu_seqlens and cu_seqlens_host are both NULL");
+    if (T > 0) {
+        if (!q || !k || !v || !g_raw || !beta_raw || !out)
+            return fail(KDA_ERR_INVALID_ARG, "a q/k/v/g_raw/beta_raw/out pointer is NULL");
+        const void* p16[] = {q, k, v, g_raw, out};
+        const char* n16[] = {"q", "k", "v", "g_raw", "out"};
+        for (int i = 0; i < 5; ++i)
+            if (!aligned(p16[i], 16))
+                return fail(KDA_ERR_UNSUPPORTED, "%s is not 16-byte aligned", n16[i]);
+        if (!aligned(beta_raw, 4)) return fail(KDA_ERR_UNSUPPORTED, "beta_raw is not 4-byte aligned");
+        const size_t act = (size_t)T * H * kD * 2;
+        Range ro = rng("out", out, act);
+        Range ins[] = {rng("q", q, act), rng("k", k, act), rng("v", v, act),
+                       rng("g_raw", g_raw, act * 2), rng("beta_raw", beta_raw, (size_t)T * H * 4)};
+        for (auto& r : ins)
+            if (overlaps(ro, r)) return fail(KDA_ERR_INVALID_ARG, "out overlaps %s", r.name);
+    }
+    if (cu_host) {
+        int rc = check_host_bounds(cu_host, N, T);
+        if (rc != KDA_OK) return rc;
+    }
+    const size_t need = kda_workspace_size(T, N, H);
+    if (need > 0 && (!workspace || workspace_bytes < need))
+        return fail(KDA_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed",
+                    workspace ? workspace_bytes : (size_t)0, need);
+    if (workspace && !aligned(workspace, 256))
+        return fail(KDA_ERR_UNSUPPORTED, "workspace is not 256-byte aligned");
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_chunk_size(void) { return kChunk; }
+
+size_t kda_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_t num_heads) {
+    if (total_tokens < 0 || num_seqs < 0 || num_heads <= 0) return 0;
+    if (num_seqs == 0) return 0;
+    return kda::workspace_layout(max_chunks(total_tokens, num_seqs), num_heads).total;
+}
+
+const char* kda_last_error(void) { return g_err.c_str(); }
+
+int kda_plan_chunks(const int32_t* cu, int32_t N, int32_t chunk_size, int32_t* chunk_seq,
+                    int32_t* chunk_in_seq, int32_t* seq_chunk_offset, int64_t capacity,
+                    int64_t* n_chunks) {
+    if (!cu || N < 0 || chunk_size <= 0 || !n_chunks)
+        return fail(KDA_ERR_INVALID_ARG, "invalid arguments to kda_plan_chunks");
+    if (cu[0] != 0) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens_host[0] != 0");
+    int64_t total = 0;
+    for (int32_t n = 0; n < N; ++n) {
+        if (cu[n + 1] < cu[n]) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens_host decreases at %d", n);
+        total += ((int64_t)cu[n + 1] - cu[n] + chunk_size - 1) / chunk_size;
+    }
+    *n_chunks = total;
+    if (total > capacity) return fail(KDA_ERR_WORKSPACE, "capacity %lld < %lld chunks",
+                                      (long long)capacity, (long long)total);
+    int64_t j = 0;
+    for (int32_t n = 0; n < N; ++n) {
+        if (seq_chunk_offset) seq_chunk_offset[n] = (int32_t)j;
+        const int64_t nc = ((int64_t)cu[n + 1] - cu[n] + chunk_size - 1) / chunk_size;
+        for (int64_t c = 0; c < nc; ++c, ++j) {
+            if (chunk_seq) chunk_seq[j] = n;
+            if (chunk_in_seq) chunk_in_seq[j] = (int32_t)c;
+        }
+    }
+    if (seq_chunk_offset) seq_chunk_offset[N] = (int32_t)j;
+    return KDA_OK;
+}
+
+int kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g_raw,
+                  const float* beta_raw, const int32_t* cu_seqlens,
+                  const int32_t* cu_seqlens_host, int32_t num_seqs, int64_t total_tokens,
+                  int32_t num_heads, void* state_cache, int64_t state_stride0,
+                  int32_t num_slots, const int32_t* state_indices,
+                  const uint8_t* has_initial_state, void* out, float lower_bound,
+                  int state_dtype, void* workspace, size_t workspace_bytes,
+                  kda_stream_t stream) {
+    int rc = common_checks(q, k, v, g_raw, beta_raw, cu_seqlens, cu_seqlens_host, num_seqs,
+                           total_tokens, num_heads, out, lower_bound, state_dtype, workspace,
+                           workspace_bytes);
+    if (rc != KDA_OK) return rc;
+    const int64_t plane = (int64_t)num_heads * kD * kD;
+    if (num_seqs > 0) {
+        if (!state_cache || !state_indices || !has_initial_state)
+            return fail(KDA_ERR_INVALID_ARG,
+                        "state_cache, state_indices and has_initial_state are required");
+        if (num_slots <= 0) return fail(KDA_ERR_INVALID_ARG, "num_slots = %d", num_slots);
+        if (num_slots < num_seqs)
+            return fail(KDA_ERR_INVALID_ARG, "num_slots %d < num_seqs %d (slots are distinct)",
+                        num_slots, num_seqs);
+        if (state_stride0 < plane)
+            return fail(KDA_ERR_INVALID_ARG,
+                        "state_stride0 %lld is smaller than the slot plane H*V*K = %lld",
+                        (long long)state_stride0, (long long)plane);
+        const size_t elt = state_elt(state_dtype);
+        if (!aligned(state_cache, 16) || ((size_t)state_stride0 * elt) % 16 != 0)
+            return fail(KDA_ERR_UNSUPPORTED,
+                        "state_cache and its slot stride must be 16-byte aligned");
+        const size_t pool_bytes = ((size_t)(num_slots - 1) * state_stride0 + plane) * elt;
+        Range rp = rng("state_cache", state_cache, pool_bytes);
+        const size_t act = (size_t)total_tokens * num_heads * kD * 2;
+        Range others[] = {rng("q", q, act), rng("k", k, act), rng("v", v, act),
+                          rng("g_raw", g_raw, act * 2),
+                          rng("beta_raw", beta_raw, (size_t)total_tokens * num_heads * 4),
+                          rng("out", out, act)};
+        for (auto& r : others)
+            if (overlaps(rp, r)) return fail(KDA_ERR_INVALID_ARG, "state_cache overlaps %s", r.name);
+    }
+    StateArgs st{state_cache, state_cache, state_stride0, state_stride0,
+                 state_indices, state_indices, has_initial_state};
+    return run_forward(q, k, v, g_raw, beta_raw, cu_seqlens, cu_seqlens_host, num_seqs,
+                       total_tokens, num_heads, st, state_dtype, out, lower_bound, workspace,
+                       workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kda_chunk_fwd_dense(const void* q, const void* k, const void* v, const float* g_raw,
+                        const float* beta_raw, const int32_t* cu_seqlens,
+                        const int32_t* cu_seqlens_host, int32_t num_seqs,
+                        int64_t total_tokens, int32_t num_heads, const void* initial_state,
+                        const uint8_t* has_initial_state, void* final_state, int state_dtype,
+                        void* out, float lower_bound, void* workspace,
+                        size_t workspace_bytes, kda_stream_t stream) {
+    int rc = common_checks(q, k, v, g_raw, beta_raw, cu_seqlens, cu_seqlens_host, num_seqs,
+                           total_tokens, num_heads, out, lower_bound, state_dtype, workspace,
+                           workspace_bytes);
+    if (rc != KDA_OK) return rc;
+    const int64_t plane = (int64_t)num_heads * kD * kD;
+    if (num_seqs > 0) {
+        if (!final_state) return fail(KDA_ERR_INVALID_ARG, "final_state is NULL");
+        if (has_initial_state && !initial_state)
+            return fail(KDA_ERR_INVALID_ARG, "has_initial_state given without initial_state");
+        if (!aligned(final_state, 16) || (initial_state && !aligned(initial_state, 16)))
+            return fail(KDA_ERR_UNSUPPORTED, "state buffers must be 16-byte aligned");
+        const size_t bytes = (size_t)num_seqs * plane * state_elt(state_dtype);
+        Range rf = rng("final_state", final_state, bytes);
+        const size_t act = (size_t)total_tokens * num_heads * kD * 2;
+        Range others[] = {rng("q", q, act), rng("k", k, act), rng("v", v, act),
+                          rng("g_raw", g_raw, act * 2),
+                          rng("beta_raw", beta_raw, (size_t)total_tokens * num_heads * 4),
+                          rng("out", out, act)};
+        for (auto& r : others)
+            if (overlaps(rf, r)) return fail(KDA_ERR_INVALID_ARG, "final_state overlaps %s", r.name);
+        if (initial_state && initial_state != final_state &&
+            overlaps(rf, rng("initial_state", initial_state, bytes)))
+            return fail(KDA_ERR_INVALID_ARG, "final_state partially overlaps initial_state");
+    }
+    StateArgs st{initial_state, final_state, plane, plane, nullptr, nullptr, has_initial_state};
+    return run_forward(q, k, v, g_raw, beta_raw, cu_seqlens, cu_seqlens_host, num_seqs,
+                       total_tokens, num_heads, st, state_dtype, out, lower_bound, workspace,
+                       workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kda_release_cache(void) {
+    std::lock_guard<std::mutex> lock(cache().mu);
+    int rc = cache().release();
+    return rc == KDA_OK ? KDA_OK : fail(rc, "cudaDeviceSynchronize failed during release");
+}
+
+int kda_cache_entries(void) {
+    std::lock_guard<std::mutex> lock(cache().mu);
+    return (int)cache().map.size();
+}
+
+int kda_set_kernel_timing(int enable) {
+    std::lock_guard<std::mutex> lock(cache().mu);
+    timing().enabled = enable != 0;
+    return KDA_OK;
+}
+
+int kda_kernel_times(float* ms, int capacity, int* count, int* calls) {
+    std::lock_guard<std::mutex> lock(cache().mu);
+    if (!ms || !count || !calls || capacity < kda::kNumKernels)
+        return fail(KDA_ERR_INVALID_ARG, "kda_kernel_times needs room for %d kernels",
+                    kda::kNumKernels);
+    for (int i = 0; i < kda::kNumKernels; ++i) ms[i] = 0.f;
+    Timing& t = timing();
+    int rc = KDA_OK;
+    for (auto& c : t.calls) {
+        cudaError_t e = cudaEventSynchronize(c.back());
+        if (e != cudaSuccess) rc = cuda_fail(e, "cudaEventSynchronize");
+        for (int i = 0; i < kda::kNumKernels && rc == KDA_OK; ++i) {
+            float x = 0.f;
+            e = cudaEventElapsedTime(&x, c[i], c[i + 1]);
+            if (e != cudaSuccess) rc = cuda_fail(e, "cudaEventElapsedTime");
+            ms[i] += x;
+        }
+        for (cudaEvent_t ev : c) t.free_events.push_back(ev);
+    }
+    *calls = (int)t.calls.size();
+    *count = kda::kNumKernels;
+    t.calls.clear();
+    return rc;
+}
+
+const char* kda_kernel_name(int i) { return kda::kernel_name(i); }
+
+}  // extern "C"

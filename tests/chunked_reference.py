@@ -1,0 +1,68 @@
+"""Chunked fp64 staging reference (tests only).
+
+Evaluates the chunkwise form of the gated delta rule that the CUDA kernels
+implement, step by step, in fp64 numpy: the per-chunk decay-weighted tiles,
+the unit-lower-triangular solve, w and u, then the serial walk over chunks.
+It is checked against the token-by-token oracle, which pins the chunk algebra
+independently of the GPU; the GPU tests can diff intermediate tiles with it.
+
+Inside a chunk with cumulative log-decay G_i (per channel) and incoming S_0:
+  A_kk[i,j] = b_i sum_c k_ic k_jc e^{G_ic-G_jc} (j<i),  A_qk[i,j] (j<=i) alike with q_i
+  T = (I + A_kk)^{-1},  w = T (b k e^G),  u = T (b v)
+  U = u - w S_0^T,  o = (q e^G) S_0^T + A_qk U,  S_C = S_0 Diag(e^{G_C}) + U^T (k e^{G_C-G})
+"""
+import numpy as np
+
+
+def _sig(x):
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def chunk_tiles(q, k, v, g_raw, beta_raw, lb, eps=1e-6):
+    """One chunk of one head (rows already padded with zeros / beta 0 / g 0)."""
+    C, K = q.shape
+    qn = q / np.sqrt((q * q).sum(1, keepdims=True) + eps) / np.sqrt(K)
+    kn = k / np.sqrt((k * k).sum(1, keepdims=True) + eps)
+    g = lb * _sig(g_raw)
+    b = _sig(beta_raw)
+    G = np.cumsum(g, axis=0)
+    diff = G[:, None, :] - G[None, :, :]               # [i, j, c]
+    mask_l = np.tril(np.ones((C, C), bool), -1)
+    mask_le = np.tril(np.ones((C, C), bool), 0)
+    E = np.exp(np.where(mask_le[:, :, None], diff, -np.inf))
+    Akk = b[:, None] * np.einsum("ic,jc,ijc->ij", kn, kn, E) * mask_l
+    Aqk = np.einsum("ic,jc,ijc->ij", qn, kn, E) * mask_le
+    Tm = np.linalg.inv(np.eye(C) + Akk)
+    w = Tm @ (b[:, None] * kn * np.exp(G))
+    u = Tm @ (b[:, None] * v)
+    qg = qn * np.exp(G)
+    kg = kn * np.exp(G[-1][None, :] - G)
+    gamma = np.exp(G[-1])
+    return dict(Akk=Akk, Aqk=Aqk, T=Tm, w=w, u=u, qg=qg, kg=kg, gamma=gamma)
+
+
+def forward(q, k, v, g_raw, beta_raw, cu, init, flags, lb, C=64, eps=1e-6):
+    T_, H, K = q.shape
+    V = v.shape[2]
+    N = len(cu) - 1
+    out = np.zeros((T_, H, V))
+    fin = np.zeros((N, H, V, K))
+    for n in range(N):
+        for h in range(H):
+            S = init[n, h].copy() if flags[n] else np.zeros((V, K))
+            for t0 in range(cu[n], cu[n + 1], C):
+                L = min(C, cu[n + 1] - t0)
+                pad = lambda x, fill=0.0: np.concatenate(
+                    [x, np.full((C - L,) + x.shape[1:], fill)]) if L < C else x
+                qq = pad(q[t0:t0 + L, h])
+                kk = pad(k[t0:t0 + L, h])
+                vv = pad(v[t0:t0 + L, h])
+                gg = pad(g_raw[t0:t0 + L, h], -np.inf)   # g = 0 on padded rows
+                bb = pad(beta_raw[t0:t0 + L, h], -np.inf)  # beta = 0 on padded rows
+                tl = chunk_tiles(qq, kk, vv, gg, bb, lb, eps)
+                U = tl["u"] - tl["w"] @ S.T
+                o = tl["qg"] @ S.T + tl["Aqk"] @ U
+                out[t0:t0 + L, h] = o[:L]
+                S = S * tl["gamma"][None, :] + U.T @ tl["kg"]
+            fin[n, h] = S
+    return out, fin
