@@ -429,9 +429,7 @@ int run_forward(const void* q, const void* k, const void* v, const float* g_raw,
     int rc = cache().get(cu_host, N, stream, capturing, &m);
     if (rc != KDA_OK) return rc;
 
-    const int64_t bound = max_chunks(T, N);
-    const kda::WsLayout L = kda::workspace_layout(bound, H);
-    char* ws = static_cast<char*>(workspace);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
 
     kda::FwdParams p{};
     p.q = static_cast<const __nv_bfloat16*>(q);
@@ -449,12 +447,8 @@ int run_forward(const void* q, const void* k, const void* v, const float* g_raw,
     p.seq_off = m->dev + m->layout.off_seq_off;
     p.chunk_seq = m->dev + m->layout.off_chunk_seq;
     p.chunk_tok = m->dev + m->layout.off_chunk_tok;
-    p.ws_w = reinterpret_cast<float*>(ws + L.off_w);
-    p.ws_qg = reinterpret_cast<float*>(ws + L.off_qg);
-    p.ws_kg = reinterpret_cast<float*>(ws + L.off_kg);
-    p.ws_u = reinterpret_cast<float*>(ws + L.off_u);
-    p.ws_aqk = reinterpret_cast<float*>(ws + L.off_aqk);
-    p.ws_gamma = reinterpret_cast<float*>(ws + L.off_gamma);
+    p.ws = ws ? ws + kda::kWsHeader : nullptr;
+    p.status = ws ? reinterpret_cast<int*>(ws) : nullptr;
     p.st_in = st.in;
     p.st_out = st.out;
     p.st_in_stride = st.in_stride;
@@ -465,6 +459,10 @@ int run_forward(const void* q, const void* k, const void* v, const float* g_raw,
     p.st_dtype = state_dtype;
     (void)workspace_bytes;
 
+    if (p.status) {
+        e = cudaMemsetAsync(p.status, 0, sizeof(int), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (status)");
+    }
     cudaEvent_t* marks = nullptr;
     std::vector<cudaEvent_t> ev;
     if (timing().enabled && !capturing) {
@@ -534,7 +532,7 @@ int kda_chunk_size(void) { return kChunk; }
 size_t kda_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_t num_heads) {
     if (total_tokens < 0 || num_seqs < 0 || num_heads <= 0) return 0;
     if (num_seqs == 0) return 0;
-    return kda::workspace_layout(max_chunks(total_tokens, num_seqs), num_heads).total;
+    return kda::workspace_bytes(max_chunks(total_tokens, num_seqs), num_heads);
 }
 
 const char* kda_last_error(void) { return g_err.c_str(); }

@@ -1,5 +1,5 @@
 // Internal interface between the host side of the C ABI (kda_api.cu) and the
-// CUDA kernels (kda_kernels.cu).  Not installed; not part of the ABI.
+// CUDA kernels.  Not installed; not part of the ABI.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -12,6 +12,28 @@ namespace kda {
 
 constexpr int kD = 128;  // K = V = head dimension
 constexpr int kC = 64;   // tokens per chunk
+
+// Workspace: one block of kWsBytes per (chunk, head), chunk-major
+// (block index = chunk * H + head).  Inside a block:
+//   w    [64][128] fp16  T (b k^ e^G)            swizzled 16-bit tile (two halves)
+//   qg   [64][128] fp16  q^ e^G                   swizzled
+//   kg   [64][128] fp16  k^ e^{G_C - G}           swizzled
+//   aqk  [64][64]  fp16  decay-weighted q^ k^T    swizzled, lower incl. diagonal
+//   gamma [128]    fp32  e^{G_C}
+//   u    [8][64][16] fp16  T (b v), one 2 KB slice per 16 value columns
+// The first kWsSharedBytes (everything but u) are read by every value slice.
+constexpr int kWsWOff = 0;
+constexpr int kWsQGOff = 16384;
+constexpr int kWsKGOff = 32768;
+constexpr int kWsAqkOff = 49152;
+constexpr int kWsGammaOff = 57344;
+constexpr int kWsSharedBytes = 57856;
+constexpr int kWsUOff = 57856;
+constexpr int kWsUSliceBytes = 2048;
+constexpr int kWsBytes = 74240;
+// Workspace header: one int status word (bit 0: a bounded wait gave up),
+// then the chunk blocks start at kWsHeader.
+constexpr int kWsHeader = 256;
 
 // Everything one forward launch sequence needs.  Device pointers unless noted.
 struct FwdParams {
@@ -33,13 +55,8 @@ struct FwdParams {
     const int32_t* chunk_seq;  // [n_chunks] sequence of each chunk
     const int32_t* chunk_tok;  // [n_chunks] first token of each chunk
 
-    // workspace tiles, one set per (chunk, head), chunk-major
-    float* ws_w;      // [n_chunks*H][C][D]   T (b k^ e^G)
-    float* ws_qg;     // [n_chunks*H][C][D]   q^ e^G
-    float* ws_kg;     // [n_chunks*H][C][D]   k^ e^{G_C - G}
-    float* ws_u;      // [n_chunks*H][C][D]   T (b v)
-    float* ws_aqk;    // [n_chunks*H][C][C]   decay-weighted q^ k^T, lower incl. diagonal
-    float* ws_gamma;  // [n_chunks*H][D]      e^{G_C}
+    uint8_t* ws;   // chunk blocks (kWsBytes each)
+    int* status;   // workspace header
 
     // state (paged: st_in == st_out == pool, idx = state_indices;
     //        dense: separate bases, idx == nullptr means identity)
@@ -53,11 +70,9 @@ struct FwdParams {
     int st_dtype;             // 0 fp32, 1 bf16, 2 fp16
 };
 
-// Workspace layout for an upper bound of chunks.
-struct WsLayout {
-    size_t off_w, off_qg, off_kg, off_u, off_aqk, off_gamma, total;
-};
-WsLayout workspace_layout(int64_t max_chunks, int H);
+inline size_t workspace_bytes(int64_t max_chunks, int H) {
+    return (size_t)kWsHeader + (size_t)max_chunks * (size_t)H * (size_t)kWsBytes;
+}
 
 // Number of kernels one forward launches, and their names (launch order).
 constexpr int kNumKernels = 2;
@@ -67,5 +82,10 @@ const char* kernel_name(int i);
 // holds kNumKernels + 1 events: marks[0] is recorded before the first kernel
 // and marks[i + 1] after kernel i.
 cudaError_t launch_forward(const FwdParams& p, cudaStream_t s, cudaEvent_t* marks);
+
+// Individual stages (kda_intra.cu, kda_scan.cu).
+cudaError_t launch_intra(const FwdParams& p, cudaStream_t s);
+cudaError_t launch_scan(const FwdParams& p, int groups, cudaStream_t s);
+int scan_groups(int N, int H, int num_sms);
 
 }  // namespace kda

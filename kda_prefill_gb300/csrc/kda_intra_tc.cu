@@ -1,0 +1,649 @@
+// Intra-chunk kernel on tensor cores: one persistent CTA per SM (512 threads),
+// each taking (chunk, head) items in chunk-major order.
+//
+// Per item (C = 64 tokens of one head), fused:
+//   prep   q^ = q / |q| / sqrt(K),  k^ = k / |k|,  a = e^{lb*sigmoid(g_raw)},
+//          b = sigmoid(beta_raw); rows past the sequence end get q^ = k^ = 0,
+//          a = 1, b = 0 (an exact no-op).
+//   tiles  A_qk[i][j] = sum_c q^_ic k^_jc e^{G_ic - G_jc} (j <= i),
+//          A_kk[i][j] = b_i sum_c k^_ic k^_jc e^{G_ic - G_jc} (j < i).
+//   solve  w = (I + A_kk)^{-1} (b k^ e^G),  u = (I + A_kk)^{-1} (b v),
+//          plus qg = q^ e^G, kg = k^ e^{G_C - G}, gamma = e^{G_C}.
+// (ROCm/aiter PR #4741, "Summary" and "Optimizations Applied": the prep pass
+// with L2 norm, gate and beta folded in, the intra-chunk tiles built so that no
+// decay factor overflows, the triangular solve and the w/u recompute.)
+//
+// Bounded tiles.  The chunk is cut into four 16-row blocks.  With P the
+// cumulative decay product inside a block (P_r = product of a over the block up
+// to row r) and E_B the total of block B, a pair (i in block I, j in block J < I)
+// is  e^{G_i - G_j} = P_i * (E_{J+1} ... E_{I-1}) * (E_J / P_j): three factors
+// that are all <= 1, so nothing overflows and an underflow only drops values
+// below 1e-38.  Off-diagonal blocks run as fp16 MMAs (m16n8k16) on those
+// factored operands.  Inside a diagonal block e^{G_i - G_j} = P_i / P_j; with
+// lower_bound >= -5 a block holds at most 80 nats of decay, so P >= e^-80 and
+// 1/P stay in fp32 range, and these blocks run as tf32 MMAs (m16n8k8) for the
+// extra mantissa the near-diagonal entries need.
+//
+// The solve is a blocked forward substitution on the right-hand sides:
+// W_I = T_II (X_I - sum_{J<I} A_IJ W_J) with the 16x16 inverses T_II computed in
+// registers; each warp owns 16 of the 256 columns of [X | Y].
+//
+// Data movement: inputs by TMA tiled loads (3-D tensor maps over [T][H][128],
+// 128-byte swizzle), double-buffered one item ahead; outputs are staged in
+// shared memory in their workspace layout and written by TMA bulk stores.
+
+#include <cuda.h>
+
+#include "kda_device.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+
+cudaError_t launch_intra_exact(const FwdParams& p, cudaStream_t s);
+
+namespace {
+
+using namespace dev;
+
+constexpr int C = kC;
+constexpr int kThreads = 512;
+
+// Shared-memory layout (bytes).  Stage s holds q, k (bf16 [64][128], swizzled
+// halves) and g (fp32 [64][128], swizzled quarters) of one item.
+constexpr int kStageBytes = 65536;
+constexpr int kQ = 0, kK = 16384, kG = 32768;
+constexpr int kV = 131072;       // v bf16 [64][128] -> b v fp16 -> u (in place)
+constexpr int kInvP = 147456;    // 1/P fp32 [64][128]; then the qg, kg tiles (fp16) to store
+constexpr int kLQ = 180224;      // q^ P fp16, rows 16..63 ([48][128])
+constexpr int kLK = 192512;      // k^ P fp16, rows 16..63
+constexpr int kRO = 204800;      // k^ E_B/P fp16, rows 0..47
+constexpr int kSc = 217088;      // rq[64] rk[64] beta[64] | EB, F1, F2 [4][128] (fp32)
+constexpr int kBar = kSc + 768 + 3 * 2048;
+constexpr int kSmemBytes = kBar + 64;
+// After the A-tile MMAs the LQ/LK/RO area holds the solve operands and A_qk:
+constexpr int kNAk = kLQ;               // -A_kk off-diagonal blocks, fp16 [64][64] (8 KB)
+constexpr int kAkd = kLQ + 8192;        // A_kk diagonal blocks, fp32 [4][16][16] (4 KB)
+constexpr int kT16 = kLQ + 12288;       // T_II diagonal blocks, fp16 [64][64] tile (8 KB)
+constexpr int kAqkStage = kLQ + 20480;  // A_qk, fp16 [64][64] tile (8 KB), to store
+// The P area of the current stage finally holds u ([8][64][16] fp16) to store.
+
+struct IntraMaps {
+    CUtensorMap q, k, v, g;
+};
+
+__device__ __forceinline__ float bf(const uint8_t* base, int r, int c) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(base + sw128_off(r, c, 64)));
+}
+__device__ __forceinline__ float f32t(const uint8_t* base, int r, int c) {
+    return *reinterpret_cast<const float*>(base + sw128f_off(r, c, 64));
+}
+
+__device__ __forceinline__ float sumsq_bf16x8(const uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
+        s = fmaf(lo, lo, fmaf(hi, hi, s));
+    }
+    return s;
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float* o) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        o[2 * i] = __uint_as_float(w[i] << 16);
+        o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    float* rq = reinterpret_cast<float*>(smem + kSc);
+    float* rk = rq + 64;
+    float* beta = rk + 64;
+    float* EB = beta + 64;  // [4][128] decay total of each 16-row block
+    float* F1 = EB + 512;   // [4][128] decay of the blocks before B (e^G at the block start)
+    float* F2 = F1 + 512;   // [4][128] E_B times the decay of the blocks after B
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBar);  // [0,1] inputs, [2] v
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int g8 = lane >> 2, tq = lane & 3;
+    const int mi = lane >> 3, rr = lane & 7;
+    const int H = p.H;
+    const int n_items = p.n_chunks * H;
+    const float lb = p.lower_bound;
+
+    if ((smem_u32(smem) & 1023) != 0) {  // swizzled TMA tiles need 1 KB alignment
+        if (tid == 0 && p.status) atomicOr(p.status, 2);
+        return;
+    }
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        mbar_init(&bar[2], 1);
+        fence_mbar_init();
+        prefetch_tmap(&maps.q);
+        prefetch_tmap(&maps.k);
+        prefetch_tmap(&maps.v);
+        prefetch_tmap(&maps.g);
+    }
+    __syncthreads();
+
+    // TMA issue (thread 0).
+    auto issue_inputs = [&](int it, int stage) {
+        uint8_t* st = smem + stage * kStageBytes;
+        const int t0 = p.chunk_tok[it / H], h = it % H;
+        mbar_arrive_expect_tx(&bar[stage], 65536);
+        tma_load_3d(st + kQ, &maps.q, &bar[stage], 0, h, t0);
+        tma_load_3d(st + kQ + 8192, &maps.q, &bar[stage], 64, h, t0);
+        tma_load_3d(st + kK, &maps.k, &bar[stage], 0, h, t0);
+        tma_load_3d(st + kK + 8192, &maps.k, &bar[stage], 64, h, t0);
+#pragma unroll
+        for (int qt = 0; qt < 4; ++qt)
+            tma_load_3d(st + kG + qt * 8192, &maps.g, &bar[stage], 32 * qt, h, t0);
+    };
+    auto issue_v = [&](int it) {
+        const int t0 = p.chunk_tok[it / H], h = it % H;
+        mbar_arrive_expect_tx(&bar[2], 16384);
+        tma_load_3d(smem + kV, &maps.v, &bar[2], 0, h, t0);
+        tma_load_3d(smem + kV + 8192, &maps.v, &bar[2], 64, h, t0);
+    };
+    auto load_braw = [&](int it) -> float {
+        const int ch = it / H, hh = it % H;
+        const int t0 = p.chunk_tok[ch];
+        const int ln = min(C, p.cu[p.chunk_seq[ch] + 1] - t0);
+        return (tid < ln) ? p.beta_raw[(size_t)(t0 + tid) * H + hh] : 0.f;
+    };
+
+    const int first = blockIdx.x;
+    if (tid == 0 && first < n_items) issue_inputs(first, 0);
+    float braw_next = (tid < C && first < n_items) ? load_braw(first) : 0.f;
+
+    int n_local = 0;
+    for (int it = first; it < n_items; it += gridDim.x, ++n_local) {
+        const int stage = n_local & 1;
+        const int chunk = it / H, h = it % H;
+        const int tok0 = p.chunk_tok[chunk];
+        const int seq = p.chunk_seq[chunk];
+        const int len = min(C, p.cu[seq + 1] - tok0);
+        uint8_t* st = smem + stage * kStageBytes;
+        uint8_t* blk = p.ws + (size_t)it * kWsBytes;
+        const int nxt = it + gridDim.x;
+        (void)h;
+
+        if (tid == 0) {
+            bulk_wait_read_all();  // the previous item's stores have read their staging
+            issue_v(it);
+            if (nxt < n_items) issue_inputs(nxt, stage ^ 1);
+        }
+        const float braw = braw_next;
+        if (tid < C && nxt < n_items) braw_next = load_braw(nxt);
+
+        const bool ok_in = mbar_wait(&bar[stage], (n_local >> 1) & 1);
+        if (__syncthreads_or(!ok_in)) {
+            if (tid == 0 && p.status) atomicOr(p.status, 1);
+            break;
+        }
+
+        // ---- row norms (4 rows per warp, 8 lanes per row) and beta ---------
+        {
+            const int r = 4 * warp + (lane & 3);
+            const int cg = lane >> 2;
+            float sq = 0.f, sk = 0.f;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int c = 16 * cg + 8 * j;
+                sq += sumsq_bf16x8(*reinterpret_cast<const uint4*>(st + kQ + sw128_off(r, c, 64)));
+                sk += sumsq_bf16x8(*reinterpret_cast<const uint4*>(st + kK + sw128_off(r, c, 64)));
+            }
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            }
+            if (cg == 0) {
+                const bool valid = r < len;
+                rq[r] = valid ? rsqrtf(sq + 1e-6f) * 0.08838834764831845f : 0.f;  // 1/sqrt(128)
+                rk[r] = valid ? rsqrtf(sk + 1e-6f) : 0.f;
+            }
+            if (tid < C) beta[tid] = (tid < len) ? __fdividef(1.f, 1.f + __expf(-braw)) : 0.f;
+        }
+        __syncthreads();
+
+        // ---- decay products per (16-row block, channel) -----------------------
+        //   forward: a = e^{lb sigmoid(g)}, P (in place of g), q^ P and k^ P (left
+        //   operands); backward: R = P_end / P (suffix product), 1/P = R / P_end,
+        //   k^ R (right operand of the off-diagonal blocks).
+        {
+            const int B = tid >> 7, c = tid & 127;
+            float P = 1.f;
+            float a[16], kh[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int r = 16 * B + i;
+                float* gp = reinterpret_cast<float*>(st + kG + sw128f_off(r, c, 64));
+                const float sg = __fdividef(1.f, 1.f + __expf(-*gp));
+                a[i] = (r < len) ? __expf(lb * sg) : 1.f;
+                P *= a[i];
+                *gp = P;
+                const float qh = bf(st + kQ, r, c) * rq[r];
+                kh[i] = bf(st + kK, r, c) * rk[r];
+                if (B >= 1) {
+                    *reinterpret_cast<__half*>(smem + kLQ + sw128_off(r - 16, c, 48)) =
+                        __float2half_rn(qh * P);
+                    *reinterpret_cast<__half*>(smem + kLK + sw128_off(r - 16, c, 48)) =
+                        __float2half_rn(kh[i] * P);
+                }
+            }
+            EB[B * 128 + c] = P;
+            const float inv_end = __fdividef(1.f, P);
+            float R = 1.f;
+#pragma unroll
+            for (int i = 15; i >= 0; --i) {
+                const int r = 16 * B + i;
+                *reinterpret_cast<float*>(smem + kInvP + sw128f_off(r, c, 64)) = R * inv_end;
+                if (B <= 2)
+                    *reinterpret_cast<__half*>(smem + kRO + sw128_off(r, c, 48)) =
+                        __float2half_rn(kh[i] * R);
+                R *= a[i];
+            }
+        }
+        __syncthreads();
+
+        // ---- A tiles (warps 0-7), overlapped with the qg/kg/X pass (warps 8-15) ----
+        float accD[2][2][4] = {};  // diagonal warps: [q/k][nt][e]
+        float accO[3][2][4] = {};  // off-diagonal warps: three block pairs
+        uint32_t xo[2][3][8];      // X-pass warps: [pass][qg/kg/X][half2 pairs]
+        if (warp < 4) {
+            // diagonal block I = warp, tf32 (m16n8k8) on P-factored operands
+            const int I = warp;
+            const int r0 = 16 * I + g8, r1 = r0 + 8;
+            const float rq0 = rq[r0], rq1 = rq[r1], rk0 = rk[r0], rk1 = rk[r1];
+#pragma unroll 4
+            for (int ks = 0; ks < 16; ++ks) {
+                const int cl = 8 * ks + tq, ch = cl + 4;
+                const float P00 = f32t(st + kG, r0, cl), P10 = f32t(st + kG, r1, cl);
+                const float P01 = f32t(st + kG, r0, ch), P11 = f32t(st + kG, r1, ch);
+                uint32_t aq[4], ak[4], b[2][2];
+                aq[0] = to_tf32(bf(st + kQ, r0, cl) * rq0 * P00);
+                aq[1] = to_tf32(bf(st + kQ, r1, cl) * rq1 * P10);
+                aq[2] = to_tf32(bf(st + kQ, r0, ch) * rq0 * P01);
+                aq[3] = to_tf32(bf(st + kQ, r1, ch) * rq1 * P11);
+                ak[0] = to_tf32(bf(st + kK, r0, cl) * rk0 * P00);
+                ak[1] = to_tf32(bf(st + kK, r1, cl) * rk1 * P10);
+                ak[2] = to_tf32(bf(st + kK, r0, ch) * rk0 * P01);
+                ak[3] = to_tf32(bf(st + kK, r1, ch) * rk1 * P11);
+                // B columns j = rows r0 (n-tile 0) and r1 (n-tile 1): k^_j / P_j
+                b[0][0] = to_tf32(bf(st + kK, r0, cl) * rk0 * f32t(smem + kInvP, r0, cl));
+                b[0][1] = to_tf32(bf(st + kK, r0, ch) * rk0 * f32t(smem + kInvP, r0, ch));
+                b[1][0] = to_tf32(bf(st + kK, r1, cl) * rk1 * f32t(smem + kInvP, r1, cl));
+                b[1][1] = to_tf32(bf(st + kK, r1, ch) * rk1 * f32t(smem + kInvP, r1, ch));
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    mma_tf32(accD[0][nt], aq, b[nt][0], b[nt][1]);
+                    mma_tf32(accD[1][nt], ak, b[nt][0], b[nt][1]);
+                }
+            }
+        } else if (warp < 8) {
+            // off-diagonal block pairs, fp16 (m16n8k16) on bounded operands;
+            // items in order (1,0) (2,0) (2,1) (3,0) (3,1) (3,2), q-left then k-left
+            const uint32_t rt = smem_u32(smem + kRO);
+#pragma unroll
+            for (int q3 = 0; q3 < 3; ++q3) {
+                const int itm = (warp - 4) * 3 + q3;
+                const int pi = itm >> 1, which = itm & 1;
+                const int tI = pi < 1 ? 1 : (pi < 3 ? 2 : 3);
+                const int tJ = pi - tI * (tI - 1) / 2;
+                const uint32_t lt = smem_u32(smem + (which ? kLK : kLQ));
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    uint32_t a4[4], b4[4];
+                    ldsm_x4(lt + sw128_off(16 * (tI - 1) + rr + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1),
+                                           48),
+                            a4[0], a4[1], a4[2], a4[3]);
+                    if (tI - tJ >= 2) {
+                        const int cc = 16 * ks + 2 * tq;
+                        float m0 = 1.f, m1 = 1.f, m8 = 1.f, m9 = 1.f;
+                        for (int Bm = tJ + 1; Bm < tI; ++Bm) {
+                            m0 *= EB[Bm * 128 + cc];
+                            m1 *= EB[Bm * 128 + cc + 1];
+                            m8 *= EB[Bm * 128 + cc + 8];
+                            m9 *= EB[Bm * 128 + cc + 9];
+                        }
+                        const __half2 mlo = __floats2half2_rn(m0, m1);
+                        const __half2 mhi = __floats2half2_rn(m8, m9);
+                        __half2* ah = reinterpret_cast<__half2*>(a4);
+                        ah[0] = __hmul2(ah[0], mlo);
+                        ah[1] = __hmul2(ah[1], mlo);
+                        ah[2] = __hmul2(ah[2], mhi);
+                        ah[3] = __hmul2(ah[3], mhi);
+                    }
+                    ldsm_x4(rt + sw128_off(16 * tJ + rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1), 48),
+                            b4[0], b4[1], b4[2], b4[3]);
+                    mma_f16(accO[q3][0], a4, b4[0], b4[1]);
+                    mma_f16(accO[q3][1], a4, b4[2], b4[3]);
+                }
+            }
+        } else {
+            // block-level decay factors and gamma, then qg, kg, X into registers
+            const int t2 = tid - 256;
+            for (int e = t2; e < 512; e += 256) {
+                const int Bq = e >> 7, cq = e & 127;
+                float pre = 1.f, suf = 1.f;
+#pragma unroll
+                for (int Bm = 0; Bm < 4; ++Bm) {
+                    const float x = EB[Bm * 128 + cq];
+                    if (Bm < Bq) pre *= x;
+                    if (Bm > Bq) suf *= x;
+                }
+                F1[e] = pre;
+                F2[e] = EB[e] * suf;
+                if (Bq == 0) reinterpret_cast<float*>(blk + kWsGammaOff)[cq] = EB[e] * suf;
+            }
+            asm volatile("bar.sync 2, 256;" ::: "memory");
+            const int r = (lane & 7) + 8 * (t2 >> 5);  // 8 consecutive lanes: 8 rows
+            const int cg = lane >> 3;                   // 32-channel group
+            const int Br = r >> 4;
+            const float qs = rq[r], ksc = rk[r], bt = beta[r];
+#pragma unroll
+            for (int pass = 0; pass < 2; ++pass) {
+                const int c0 = 32 * cg + 16 * pass;
+                float Pv[16], Iv[16], qv[16], kv[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    *reinterpret_cast<float4*>(Pv + 4 * j) =
+                        *reinterpret_cast<const float4*>(st + kG + sw128f_off(r, c0 + 4 * j, 64));
+                    *reinterpret_cast<float4*>(Iv + 4 * j) =
+                        *reinterpret_cast<const float4*>(smem + kInvP + sw128f_off(r, c0 + 4 * j, 64));
+                }
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    bf16x8_to_f32(*reinterpret_cast<const uint4*>(st + kQ + sw128_off(r, c0 + 8 * j, 64)),
+                                  qv + 8 * j);
+                    bf16x8_to_f32(*reinterpret_cast<const uint4*>(st + kK + sw128_off(r, c0 + 8 * j, 64)),
+                                  kv + 8 * j);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float o[3][2];
+#pragma unroll
+                    for (int e2 = 0; e2 < 2; ++e2) {
+                        const int e = 2 * j + e2;
+                        const float f1 = F1[Br * 128 + c0 + e], f2 = F2[Br * 128 + c0 + e];
+                        const float qh = qv[e] * qs, kh = kv[e] * ksc;
+                        const float eG = f1 * Pv[e];
+                        o[0][e2] = qh * eG;             // qg
+                        o[1][e2] = kh * Iv[e] * f2;     // kg
+                        o[2][e2] = bt * kh * eG;        // X
+                    }
+                    xo[pass][0][j] = pack_half2(o[0][0], o[0][1]);
+                    xo[pass][1][j] = pack_half2(o[1][0], o[1][1]);
+                    xo[pass][2][j] = pack_half2(o[2][0], o[2][1]);
+                }
+            }
+        }
+        __syncthreads();  // every read of q, k, P, 1/P and the LQ/LK/RO operands is done
+
+        // ---- stage qg, kg (in the 1/P area), X (in place of q), A tiles ---------
+        if (warp >= 8) {
+            const int t2 = tid - 256;
+            const int r = (lane & 7) + 8 * (t2 >> 5);
+            const int cg = lane >> 3;
+#pragma unroll
+            for (int pass = 0; pass < 2; ++pass) {
+                const int c0 = 32 * cg + 16 * pass;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const uint32_t o = sw128_off(r, c0 + 8 * j, 64);
+                    *reinterpret_cast<uint4*>(smem + kInvP + o) =
+                        make_uint4(xo[pass][0][4 * j], xo[pass][0][4 * j + 1], xo[pass][0][4 * j + 2],
+                                   xo[pass][0][4 * j + 3]);
+                    *reinterpret_cast<uint4*>(smem + kInvP + 16384 + o) =
+                        make_uint4(xo[pass][1][4 * j], xo[pass][1][4 * j + 1], xo[pass][1][4 * j + 2],
+                                   xo[pass][1][4 * j + 3]);
+                    *reinterpret_cast<uint4*>(st + kQ + o) =
+                        make_uint4(xo[pass][2][4 * j], xo[pass][2][4 * j + 1], xo[pass][2][4 * j + 2],
+                                   xo[pass][2][4 * j + 3]);
+                }
+            }
+        } else {
+            // A_qk (j <= i) -> staging tile; A_kk (j < i, times beta_i): diagonal
+            // blocks fp32, off-diagonal blocks negated fp16.
+            auto put = [&](int sel, int tI, int tJ, const float (&acc)[2][4]) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int i = 16 * tI + g8 + 8 * hh;
+                        const int j = 16 * tJ + 8 * nt + 2 * tq;
+                        float x0 = acc[nt][2 * hh], x1 = acc[nt][2 * hh + 1];
+                        if (sel == 0) {
+                            if (tI == tJ) {
+                                if (j > i) x0 = 0.f;
+                                if (j + 1 > i) x1 = 0.f;
+                            }
+                            *reinterpret_cast<uint32_t*>(smem + kAqkStage + sw64_off(i, j)) =
+                                pack_half2(x0, x1);
+                        } else if (tI == tJ) {
+                            float* d = reinterpret_cast<float*>(smem + kAkd) + tI * 256;
+                            const float bi = beta[i];
+                            d[(i & 15) * 16 + (j & 15)] = (j >= i) ? 0.f : bi * x0;
+                            d[(i & 15) * 16 + (j & 15) + 1] = (j + 1 >= i) ? 0.f : bi * x1;
+                        } else {
+                            const float bi = -beta[i];
+                            *reinterpret_cast<uint32_t*>(smem + kNAk + sw64_off(i, j)) =
+                                pack_half2(bi * x0, bi * x1);
+                        }
+                    }
+            };
+            if (warp < 4) {
+                put(0, warp, warp, accD[0]);
+                put(1, warp, warp, accD[1]);
+            } else {
+#pragma unroll
+                for (int q3 = 0; q3 < 3; ++q3) {
+                    const int itm = (warp - 4) * 3 + q3;
+                    const int pi = itm >> 1, which = itm & 1;
+                    const int tI = pi < 1 ? 1 : (pi < 3 ? 2 : 3);
+                    const int tJ = pi - tI * (tI - 1) / 2;
+                    put(which, tI, tJ, accO[q3]);
+                }
+            }
+        }
+        fence_proxy_async();
+        __syncthreads();
+        if (tid == 0) {
+            bulk_s2g(blk + kWsQGOff, smem + kInvP, 32768);  // qg and kg are adjacent
+            bulk_s2g(blk + kWsAqkOff, smem + kAqkStage, 8192);
+            bulk_commit();
+        }
+
+        // ---- diagonal inverses T_II = (I + A_II)^{-1} (warps 0-1, in registers)
+        //      and Y = b v in place (other warps) -------------------------------
+        if (warp < 2) {
+            const int I = 2 * warp + (lane >> 4), col = lane & 15;
+            const float* Ad = reinterpret_cast<const float*>(smem + kAkd) + I * 256;
+            float t[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float acc = (i == col) ? 1.f : 0.f;
+#pragma unroll
+                for (int j = 0; j < i; ++j) acc -= Ad[i * 16 + j] * t[j];
+                t[i] = acc;  // zero above the diagonal since t[j] = 0 for j < col
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                *reinterpret_cast<__half*>(smem + kT16 + sw64_off(16 * I + i, 16 * I + col)) =
+                    __float2half_rn(t[i]);
+        } else {
+            const bool ok_v = mbar_wait(&bar[2], n_local & 1);
+            if (!ok_v && p.status) atomicOr(p.status, 1);
+            for (int e = tid - 64; e < C * 64; e += kThreads - 64) {  // pairs of elements
+                const int r = e >> 6, c2 = (e & 63) * 2;
+                uint8_t* vp = smem + kV + sw128_off(r, c2, 64);
+                const float2 vv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vp));
+                *reinterpret_cast<uint32_t*>(vp) = pack_half2(beta[r] * vv.x, beta[r] * vv.y);
+            }
+        }
+        __syncthreads();
+
+        // ---- w = (I + A_kk)^{-1} X and u = (I + A_kk)^{-1} Y by blocked forward
+        //      substitution: R_I = X_I - sum_{J<I} A_IJ W_J, W_I = T_II R_I.  Warp
+        //      w owns 16 of the 256 columns of [X | Y]; the blocks of W overwrite
+        //      X (or Y) in place.  No CTA barrier: each warp reads only its columns.
+        {
+            const bool isu = warp >= 8;
+            const int n0 = 16 * (warp & 7);
+            uint8_t* xt = isu ? smem + kV : st + kQ;
+            const uint32_t xb = smem_u32(xt);
+            const uint32_t nak = smem_u32(smem + kNAk), t16 = smem_u32(smem + kT16);
+            uint8_t* ustage = st + kG + (warp & 7) * kWsUSliceBytes;  // [64][16] fp16
+#pragma unroll
+            for (int I = 0; I < 4; ++I) {
+                float acc[2][4];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint32_t xv = *reinterpret_cast<const uint32_t*>(
+                            xt + sw128_off(16 * I + g8 + 8 * hh, n0 + 8 * nt + 2 * tq, 64));
+                        const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&xv));
+                        acc[nt][2 * hh] = xf.x;
+                        acc[nt][2 * hh + 1] = xf.y;
+                    }
+                for (int J = 0; J < I; ++J) {
+                    uint32_t a[4], b[4];
+                    ldsm_x4(nak + sw64_off(16 * I + rr + 8 * (mi & 1), 16 * J + 8 * (mi >> 1)), a[0],
+                            a[1], a[2], a[3]);
+                    ldsm_x4_t(xb + sw128_off(16 * J + rr + 8 * (mi & 1), n0 + 8 * (mi >> 1), 64), b[0],
+                              b[1], b[2], b[3]);
+                    mma_f16(acc[0], a, b[0], b[1]);
+                    mma_f16(acc[1], a, b[2], b[3]);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh)
+                        *reinterpret_cast<uint32_t*>(
+                            xt + sw128_off(16 * I + g8 + 8 * hh, n0 + 8 * nt + 2 * tq, 64)) =
+                            pack_half2(acc[nt][2 * hh], acc[nt][2 * hh + 1]);
+                __syncwarp();
+                float wv[2][4] = {};
+                {
+                    uint32_t a[4], b[4];
+                    ldsm_x4(t16 + sw64_off(16 * I + rr + 8 * (mi & 1), 16 * I + 8 * (mi >> 1)), a[0],
+                            a[1], a[2], a[3]);
+                    ldsm_x4_t(xb + sw128_off(16 * I + rr + 8 * (mi & 1), n0 + 8 * (mi >> 1), 64), b[0],
+                              b[1], b[2], b[3]);
+                    mma_f16(wv[0], a, b[0], b[1]);
+                    mma_f16(wv[1], a, b[2], b[3]);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int i = 16 * I + g8 + 8 * hh;
+                        const int col = n0 + 8 * nt + 2 * tq;
+                        const uint32_t v2 = pack_half2(wv[nt][2 * hh], wv[nt][2 * hh + 1]);
+                        *reinterpret_cast<uint32_t*>(xt + sw128_off(i, col, 64)) = v2;
+                        if (isu)
+                            *reinterpret_cast<uint32_t*>(ustage + (i * 16 + 8 * nt + 2 * tq) * 2) = v2;
+                    }
+                __syncwarp();
+            }
+        }
+        fence_proxy_async();
+        __syncthreads();
+        if (tid == 0) {
+            bulk_s2g(blk + kWsWOff, st + kQ, 16384);
+            bulk_s2g(blk + kWsUOff, st + kG, 16384);
+            bulk_commit();
+        }
+    }
+    if (tid == 0) bulk_wait_all();  // stores complete before the CTA releases its smem
+}
+
+// ---- host side -------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elt, int box_x,
+              int H, int64_t T) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[2] = {(cuuint64_t)128 * elt, (cuuint64_t)H * 128 * elt};
+    cuuint32_t box[3] = {(cuuint32_t)box_x, 1, (cuuint32_t)C};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_intra(const FwdParams& p, cudaStream_t s) {
+    if (p.n_chunks <= 0) return cudaSuccess;
+    if (p.lower_bound < -5.0f) return launch_intra_exact(p, s);
+    IntraMaps maps;
+    if (!make_map(&maps.q, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, p.H, p.T) ||
+        !make_map(&maps.k, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, p.H, p.T) ||
+        !make_map(&maps.v, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, p.H, p.T) ||
+        !make_map(&maps.g, p.g_raw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32, p.H, p.T))
+        return cudaErrorInvalidValue;
+    static unsigned configured = 0;
+    static int sms[32] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 32 && !(configured & (1u << dev))) {
+        e = cudaFuncSetAttribute(kda_intra_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes);
+        if (e != cudaSuccess) return e;
+        cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        configured |= 1u << dev;
+    }
+    const int n_items = p.n_chunks * p.H;
+    const int grid = n_items < sms[dev < 32 ? dev : 0] ? n_items : sms[dev < 32 ? dev : 0];
+    kda_intra_tc<<<grid > 0 ? grid : 1, kThreads, kSmemBytes, s>>>(maps, p);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

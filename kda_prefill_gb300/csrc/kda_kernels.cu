@@ -1,330 +1,34 @@
-// CUDA kernels of the chunkwise KDA forward (sm_103a).
-//
-// Chunkwise form of the gated delta rule used here (derived from the token
-// recurrence S_t = S_{t-1} Diag(e^{g_t}) (I - b_t k_t k_t^T) + b_t v_t k_t^T,
-// o_t = S_t q_t).  Inside a chunk of C tokens with in-chunk cumulative
-// log-decay G_i = g_1 + ... + g_i (per channel) and incoming state S_0:
-//
-//   A_kk[i][j] = b_i sum_c k_ic k_jc e^{G_ic - G_jc}      (j < i)
-//   A_qk[i][j] =     sum_c q_ic k_jc e^{G_ic - G_jc}      (j <= i)
-//   T  = (I + A_kk)^{-1}                                   (unit lower triangular)
-//   w  = T (b k e^{G}),   u = T (b v)
-//   U  = u - w S_0^T                                       (the chunk's new values)
-//   o  = (q e^{G}) S_0^T + A_qk U
-//   S_C = S_0 Diag(e^{G_C}) + U^T (k e^{G_C - G})
-//
-// The steps follow ROCm/aiter PR #4741 ("Summary": q/k L2 norm, gate cumsum,
-// beta sigmoid, the two intra-chunk kernels, the w/u recompute, the state scan
-// and the output matmul; "Optimizations Applied": sequence-parallel split into
-// a chunk-parallel prep and a serial scan, zero padding as an exact no-op, and
-// tiles built so that no factor exceeds 1: here every decay factor is the
-// exponential of a non-positive difference G_i - G_j with j <= i).
-//
-// This file holds the first, plain SIMT fp32 version of the two kernels.
-
+// Launch sequence of one chunkwise KDA forward: the intra-chunk kernel
+// (chunk-parallel) then the state scan (serial over each sequence's chunks).
 #include "kda_internal.h"
 
 namespace kda {
-namespace {
-
-constexpr int C = kC;
-constexpr int D = kD;
-constexpr int P = D + 1;   // padded smem row pitch (floats) against bank conflicts
-constexpr int PA = C + 1;  // pitch of C x C tiles
-constexpr int kIntraThreads = 256;
-constexpr int kScanThreads = 256;
-constexpr int VS = 16;     // V rows of the state per scan CTA
-
-__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
-
-__device__ __forceinline__ float load_state(const void* base, int dtype, size_t off) {
-    if (dtype == 0) return static_cast<const float*>(base)[off];
-    if (dtype == 1) return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[off]);
-    return __half2float(static_cast<const __half*>(base)[off]);
-}
-
-__device__ __forceinline__ void store_state(void* base, int dtype, size_t off, float x) {
-    if (dtype == 0) {
-        static_cast<float*>(base)[off] = x;
-    } else if (dtype == 1) {
-        static_cast<__nv_bfloat16*>(base)[off] = __float2bfloat16_rn(x);
-    } else {
-        static_cast<__half*>(base)[off] = __float2half_rn(x);
-    }
-}
-
-constexpr size_t kIntraSmem =
-    sizeof(float) * (4 * C * P + 3 * C * PA + 3 * C);
-
-// One CTA per (chunk, head): prep (L2 norm, gate, cumsum, beta) fused with the
-// intra-chunk tiles, the triangular solve and the w/u recompute.
-__global__ void __launch_bounds__(kIntraThreads)
-kda_intra_simt(FwdParams p) {
-    extern __shared__ float sm[];
-    float* sQ = sm;             // [C][P] q, then q^
-    float* sK = sQ + C * P;     // [C][P] k, then k^
-    float* sG = sK + C * P;     // [C][P] g, then G (inclusive cumsum)
-    float* sV = sG + C * P;     // [C][P] v, then b v
-    float* sAk = sV + C * P;    // [C][PA]
-    float* sAq = sAk + C * PA;  // [C][PA]
-    float* sT = sAq + C * PA;   // [C][PA]
-    float* sB = sT + C * PA;    // [C] beta
-    float* sRq = sB + C;        // [C] 1/|q| / sqrt(K)
-    float* sRk = sRq + C;       // [C] 1/|k|
-
-    const int j = blockIdx.x;
-    const int h = blockIdx.y;
-    const int tid = threadIdx.x;
-    const int seq = p.chunk_seq[j];
-    const int tok0 = p.chunk_tok[j];
-    const int len = min(C, p.cu[seq + 1] - tok0);
-
-    for (int e = tid; e < C * D; e += kIntraThreads) {
-        const int r = e / D, c = e % D;
-        float qv = 0.f, kv = 0.f, vv = 0.f, gv = 0.f;
-        if (r < len) {
-            const size_t off = ((size_t)(tok0 + r) * p.H + h) * D + c;
-            qv = __bfloat162float(p.q[off]);
-            kv = __bfloat162float(p.k[off]);
-            vv = __bfloat162float(p.v[off]);
-            gv = p.lower_bound * sigmoidf_(p.g_raw[off]);
-        }
-        sQ[r * P + c] = qv;
-        sK[r * P + c] = kv;
-        sV[r * P + c] = vv;
-        sG[r * P + c] = gv;
-    }
-    for (int r = tid; r < C; r += kIntraThreads)
-        sB[r] = (r < len) ? sigmoidf_(p.beta_raw[(size_t)(tok0 + r) * p.H + h]) : 0.f;
-    __syncthreads();
-
-    const int warp = tid / 32, lane = tid % 32;
-    for (int r = warp; r < C; r += kIntraThreads / 32) {
-        float sq = 0.f, sk = 0.f;
-        for (int c = lane; c < D; c += 32) {
-            sq += sQ[r * P + c] * sQ[r * P + c];
-            sk += sK[r * P + c] * sK[r * P + c];
-        }
-        for (int o = 16; o > 0; o >>= 1) {
-            sq += __shfl_xor_sync(0xffffffffu, sq, o);
-            sk += __shfl_xor_sync(0xffffffffu, sk, o);
-        }
-        if (lane == 0) {
-            sRq[r] = 1.0f / sqrtf(sq + 1e-6f) / sqrtf((float)D);
-            sRk[r] = 1.0f / sqrtf(sk + 1e-6f);
-        }
-    }
-    __syncthreads();
-    for (int e = tid; e < C * D; e += kIntraThreads) {
-        const int r = e / D, c = e % D;
-        sQ[r * P + c] *= sRq[r];
-        sK[r * P + c] *= sRk[r];
-    }
-    if (tid < D) {
-        float acc = 0.f;
-        for (int r = 0; r < C; ++r) {
-            acc += sG[r * P + tid];
-            sG[r * P + tid] = acc;
-        }
-    }
-    __syncthreads();
-
-    // Decay-weighted tiles; every factor is e^{G_i - G_j} <= 1 (j <= i).
-    for (int e = tid; e < C * C; e += kIntraThreads) {
-        const int i = e / C, jj = e % C;
-        float ak = 0.f, aq = 0.f;
-        if (jj <= i) {
-            for (int c = 0; c < D; ++c) {
-                const float f = expf(sG[i * P + c] - sG[jj * P + c]) * sK[jj * P + c];
-                ak += sK[i * P + c] * f;
-                aq += sQ[i * P + c] * f;
-            }
-        }
-        sAk[i * PA + jj] = (jj < i) ? sB[i] * ak : 0.f;
-        sAq[i * PA + jj] = aq;
-    }
-    __syncthreads();
-
-    // T = (I + A_kk)^{-1} by forward substitution: T[i,:] = e_i - sum_{j<i} A[i,j] T[j,:]
-    for (int i = 0; i < C; ++i) {
-        if (tid < C) {
-            const int col = tid;
-            float acc = (col == i) ? 1.f : 0.f;
-            for (int jj = 0; jj < i; ++jj) acc -= sAk[i * PA + jj] * sT[jj * PA + col];
-            sT[i * PA + col] = (col <= i) ? acc : 0.f;
-        }
-        __syncthreads();
-    }
-
-    const size_t ch = (size_t)j * p.H + h;
-    float* gw = p.ws_w + ch * C * D;
-    float* gqg = p.ws_qg + ch * C * D;
-    float* gkg = p.ws_kg + ch * C * D;
-    float* gu = p.ws_u + ch * C * D;
-    float* gaqk = p.ws_aqk + ch * C * C;
-    float* ggam = p.ws_gamma + ch * D;
-
-    for (int e = tid; e < C * D; e += kIntraThreads) {
-        const int r = e / D, c = e % D;
-        const float G = sG[r * P + c];
-        const float GC = sG[(C - 1) * P + c];
-        gqg[e] = sQ[r * P + c] * expf(G);
-        gkg[e] = sK[r * P + c] * expf(GC - G);
-    }
-    if (tid < D) ggam[tid] = expf(sG[(C - 1) * P + tid]);
-    for (int e = tid; e < C * C; e += kIntraThreads) gaqk[e] = sAq[(e / C) * PA + (e % C)];
-    __syncthreads();
-    // reuse sQ for b k^ e^G and sV for b v
-    for (int e = tid; e < C * D; e += kIntraThreads) {
-        const int r = e / D, c = e % D;
-        sQ[r * P + c] = sB[r] * sK[r * P + c] * expf(sG[r * P + c]);
-        sV[r * P + c] = sB[r] * sV[r * P + c];
-    }
-    __syncthreads();
-    for (int e = tid; e < C * D; e += kIntraThreads) {
-        const int i = e / D, c = e % D;
-        float aw = 0.f, au = 0.f;
-        for (int jj = 0; jj <= i; ++jj) {
-            const float t = sT[i * PA + jj];
-            aw += t * sQ[jj * P + c];
-            au += t * sV[jj * P + c];
-        }
-        gw[e] = aw;
-        gu[e] = au;
-    }
-}
-
-// One CTA per (sequence, head, block of VS state rows): the serial walk over
-// the sequence's chunks, with the output product fused and the paged state
-// loaded at the start and stored at the end.
-__global__ void __launch_bounds__(kScanThreads)
-kda_scan_simt(FwdParams p) {
-    __shared__ float sS[VS][P];
-    __shared__ float sU[C][VS + 1];
-
-    const int n = blockIdx.x;
-    const int h = blockIdx.y;
-    const int v0 = blockIdx.z * VS;
-    const int tid = threadIdx.x;
-    const int tok0 = p.cu[n];
-    const int len = p.cu[n + 1] - tok0;
-    const int c0 = p.seq_off[n], c1 = p.seq_off[n + 1];
-
-    const bool has_init = p.has_init ? (p.has_init[n] != 0) : (p.st_in != nullptr);
-    const int64_t in_slot = p.st_in_idx ? p.st_in_idx[n] : n;
-    const int64_t out_slot = p.st_out_idx ? p.st_out_idx[n] : n;
-    const size_t in_base = (size_t)in_slot * p.st_in_stride + (size_t)h * D * D;
-    const size_t out_base = (size_t)out_slot * p.st_out_stride + (size_t)h * D * D;
-
-    for (int e = tid; e < VS * D; e += kScanThreads) {
-        const int vv = e / D, c = e % D;
-        sS[vv][c] = has_init ? load_state(p.st_in, p.st_dtype, in_base + (size_t)(v0 + vv) * D + c)
-                             : 0.f;
-    }
-    __syncthreads();
-
-    for (int j = c0; j < c1; ++j) {
-        const size_t ch = (size_t)j * p.H + h;
-        const float* w = p.ws_w + ch * C * D;
-        const float* qg = p.ws_qg + ch * C * D;
-        const float* kg = p.ws_kg + ch * C * D;
-        const float* u = p.ws_u + ch * C * D;
-        const float* aqk = p.ws_aqk + ch * C * C;
-        const float* gam = p.ws_gamma + ch * D;
-        const int lc = j - c0;
-        const int rows = min(C, len - lc * C);
-
-        for (int e = tid; e < C * VS; e += kScanThreads) {
-            const int i = e / VS, vv = e % VS;
-            float acc = __ldg(u + i * D + v0 + vv);
-            for (int c = 0; c < D; ++c) acc -= __ldg(w + i * D + c) * sS[vv][c];
-            sU[i][vv] = acc;
-        }
-        __syncthreads();
-
-        for (int e = tid; e < C * VS; e += kScanThreads) {
-            const int i = e / VS, vv = e % VS;
-            if (i < rows) {
-                float acc = 0.f;
-                for (int c = 0; c < D; ++c) acc += __ldg(qg + i * D + c) * sS[vv][c];
-                for (int jj = 0; jj <= i; ++jj) acc += __ldg(aqk + i * C + jj) * sU[jj][vv];
-                const size_t t = (size_t)(tok0 + lc * C + i);
-                p.out[(t * p.H + h) * D + v0 + vv] = __float2bfloat16_rn(acc);
-            }
-        }
-
-        float snew[VS * D / kScanThreads];
-#pragma unroll
-        for (int qn = 0; qn < VS * D / kScanThreads; ++qn) {
-            const int e = tid + qn * kScanThreads;
-            const int vv = e / D, c = e % D;
-            float acc = sS[vv][c] * __ldg(gam + c);
-            for (int i = 0; i < C; ++i) acc += sU[i][vv] * __ldg(kg + i * D + c);
-            snew[qn] = acc;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int qn = 0; qn < VS * D / kScanThreads; ++qn) {
-            const int e = tid + qn * kScanThreads;
-            sS[e / D][e % D] = snew[qn];
-        }
-        __syncthreads();
-    }
-
-    for (int e = tid; e < VS * D; e += kScanThreads) {
-        const int vv = e / D, c = e % D;
-        store_state(p.st_out, p.st_dtype, out_base + (size_t)(v0 + vv) * D + c, sS[vv][c]);
-    }
-}
-
-}  // namespace
-
-WsLayout workspace_layout(int64_t max_chunks, int H) {
-    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
-    const size_t chh = (size_t)max_chunks * (size_t)H;
-    WsLayout L{};
-    size_t o = 0;
-    L.off_w = o;     o = up(o + chh * C * D * sizeof(float));
-    L.off_qg = o;    o = up(o + chh * C * D * sizeof(float));
-    L.off_kg = o;    o = up(o + chh * C * D * sizeof(float));
-    L.off_u = o;     o = up(o + chh * C * D * sizeof(float));
-    L.off_aqk = o;   o = up(o + chh * C * C * sizeof(float));
-    L.off_gamma = o; o = up(o + chh * D * sizeof(float));
-    L.total = o;
-    return L;
-}
 
 const char* kernel_name(int i) {
     static const char* names[kNumKernels] = {"kda_intra", "kda_scan"};
     return (i >= 0 && i < kNumKernels) ? names[i] : nullptr;
 }
 
-cudaError_t launch_forward(const FwdParams& p, cudaStream_t s, cudaEvent_t* marks) {
-    // per-device one-time attribute setup
-    static unsigned configured_mask = 0;
+static int num_sms() {
+    static int cached[32] = {0};
     int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 32 && !(configured_mask & (1u << dev))) {
-        e = cudaFuncSetAttribute(kda_intra_simt, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kIntraSmem);
-        if (e != cudaSuccess) return e;
-        configured_mask |= 1u << dev;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev >= 32) return 148;
+    if (!cached[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = v > 0 ? v : 148;
     }
+    return cached[dev];
+}
+
+cudaError_t launch_forward(const FwdParams& p, cudaStream_t s, cudaEvent_t* marks) {
+    cudaError_t e;
     if (marks) cudaEventRecord(marks[0], s);
-    if (p.n_chunks > 0) {
-        dim3 grid((unsigned)p.n_chunks, (unsigned)p.H);
-        kda_intra_simt<<<grid, kIntraThreads, kIntraSmem, s>>>(p);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
+    e = launch_intra(p, s);
+    if (e != cudaSuccess) return e;
     if (marks) cudaEventRecord(marks[1], s);
-    if (p.N > 0) {
-        dim3 grid((unsigned)p.N, (unsigned)p.H, (unsigned)(D / VS));
-        kda_scan_simt<<<grid, kScanThreads, 0, s>>>(p);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
+    e = launch_scan(p, scan_groups(p.N, p.H, num_sms()), s);
+    if (e != cudaSuccess) return e;
     if (marks) cudaEventRecord(marks[2], s);
     return cudaSuccess;
 }
