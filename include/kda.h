@@ -214,6 +214,46 @@ KDA_API int kda_kernel_times(float* ms, int capacity, int* count, int* calls);
 /* Name of kernel i in launch order, or NULL. */
 KDA_API const char* kda_kernel_name(int i);
 
+/*
+ * kda_chunk_fwd_noalloc — the paged forward for callers that cannot allocate
+ * device memory.  The paper has no counterpart: this entry point exists for
+ * integration only.
+ *
+ * Who needs it: code that runs where device allocation is not allowed or not
+ * available, for instance a serving runtime that owns all device memory through
+ * its own fixed arena and forbids cudaMalloc after start-up, a plain-C caller
+ * with no device allocator of its own, or code that must not perturb another
+ * allocator's bookkeeping.  kda_chunk_fwd needs a caller-provided workspace
+ * and keeps a metadata cache that allocates on a miss; this call needs
+ * neither.
+ *
+ * It takes the arguments of kda_chunk_fwd without the workspace, and
+ * cu_seqlens_host is required (its values size the launch; the chunk table
+ * itself is built on the device from cu_seqlens).  Scratch memory comes from a
+ * fixed array of KDA_NOALLOC_SCRATCH_BYTES compiled into the library; every
+ * GPU that loads the library holds it until process exit.  Sizes whose need,
+ * kda_workspace_size(total_tokens, num_seqs, num_heads) plus the chunk table,
+ * exceeds that array are rejected with KDA_ERR_WORKSPACE and a message giving
+ * both numbers (64 MiB holds, e.g., a 4096-token prefill at 12 heads).
+ *
+ * The first call on a device looks up the array's device address (a CUDA
+ * runtime query, no allocation), so make the first call on each device before
+ * any stream capture.  All calls share the one array and it keeps the last
+ * call's contents: calls that overlap on the GPU race and give wrong results,
+ * so order them (one stream, or events).  It calls no cudaMalloc, cudaFree or
+ * other allocating routine.  Results equal kda_chunk_fwd's: same kernels, same
+ * chunk table.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (64ull << 20)
+KDA_API int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v,
+                                  const float* g_raw, const float* beta_raw,
+                                  const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                                  int32_t num_seqs, int64_t total_tokens, int32_t num_heads,
+                                  void* state_cache, int64_t state_stride0, int32_t num_slots,
+                                  const int32_t* state_indices, const uint8_t* has_initial_state,
+                                  void* out, float lower_bound, int state_dtype,
+                                  kda_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -36,6 +36,7 @@ EXPORTED = (
     "kda_chunk_size", "kda_workspace_size", "kda_chunk_fwd", "kda_chunk_fwd_dense",
     "kda_plan_chunks", "kda_last_error", "kda_release_cache", "kda_cache_entries",
     "kda_set_kernel_timing", "kda_kernel_times", "kda_kernel_name",
+    "kda_chunk_fwd_noalloc",
 )
 
 
@@ -96,6 +97,14 @@ def load_library(path: str = LIB_PATH):
     lib.kda_kernel_times.argtypes = [_vp, ctypes.c_int, _vp, _vp]
     lib.kda_kernel_name.restype = ctypes.c_char_p
     lib.kda_kernel_name.argtypes = [ctypes.c_int]
+    lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
+    lib.kda_chunk_fwd_noalloc.argtypes = [
+        _vp, _vp, _vp, _vp, _vp,        # q k v g_raw beta_raw
+        _vp, _vp, _i32, _i64, _i32,     # cu_seqlens cu_seqlens_host N T H
+        _vp, _i64, _i32, _vp, _vp,      # state_cache stride0 slots indices has_init
+        _vp, ctypes.c_float, ctypes.c_int,  # out lower_bound state_dtype
+        _vp,                            # stream
+    ]
     if path == LIB_PATH:
         _lib = lib
     return lib

@@ -692,3 +692,178 @@ int kda_kernel_times(float* ms, int capacity, int* count, int* calls) {
 const char* kda_kernel_name(int i) { return kda::kernel_name(i); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point: the workspace and the chunk table live in a
+// fixed array compiled into the library instead of caller- or cache-owned
+// device memory.
+// ---------------------------------------------------------------------------
+namespace {
+
+// Every device that loads the library holds this array until process exit.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {nullptr};
+
+// Device address of the scratch array on the current device.  The array's
+// name is only a host-side stand-in in host code, so the address is looked up
+// once per device (with that device current) and cached.
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(KDA_ERR_UNSUPPORTED, "device ordinal %d", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress (scratch)");
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return KDA_OK;
+}
+
+// Chunk table from the device bounds, one CTA: chunk counts, an exclusive
+// prefix sum in tiles of 1024 sequences, then each sequence's chunks.  Same
+// numbering as the host planner (chunks follow the sequence's position in
+// cu_seqlens; empty sequences own no chunk).
+__global__ void __launch_bounds__(1024) kda_noalloc_meta(const int32_t* cu, int N, int C,
+                                                         int32_t* mcu, int32_t* off,
+                                                         int32_t* cseq, int32_t* ctok) {
+    __shared__ int32_t sbuf[1024];
+    __shared__ int32_t carry;
+    const int tid = threadIdx.x;
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < N; base += 1024) {
+        const int n = base + tid;
+        const int nc = (n < N) ? (cu[n + 1] - cu[n] + C - 1) / C : 0;
+        sbuf[tid] = nc;
+        __syncthreads();
+        for (int o = 1; o < 1024; o <<= 1) {
+            const int x = (tid >= o) ? sbuf[tid - o] : 0;
+            __syncthreads();
+            sbuf[tid] += x;
+            __syncthreads();
+        }
+        const int excl = carry + sbuf[tid] - nc;
+        if (n < N) {
+            mcu[n] = cu[n];
+            off[n] = excl;
+            for (int c = 0; c < nc; ++c) {
+                cseq[excl + c] = n;
+                ctok[excl + c] = cu[n] + c * C;
+            }
+        }
+        __syncthreads();
+        if (tid == 1023) carry += sbuf[1023];
+        __syncthreads();
+    }
+    if (tid == 0) {
+        mcu[N] = cu[N];
+        off[N] = carry;
+    }
+}
+
+}  // namespace
+
+extern "C" int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v,
+                                     const float* g_raw, const float* beta_raw,
+                                     const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                                     int32_t num_seqs, int64_t total_tokens, int32_t num_heads,
+                                     void* state_cache, int64_t state_stride0, int32_t num_slots,
+                                     const int32_t* state_indices,
+                                     const uint8_t* has_initial_state, void* out,
+                                     float lower_bound, int state_dtype, kda_stream_t stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (!cu_seqlens || !cu_seqlens_host)
+        return fail(KDA_ERR_INVALID_ARG,
+                    "kda_chunk_fwd_noalloc needs both cu_seqlens and cu_seqlens_host");
+    if (num_seqs < 0 || total_tokens < 0 || num_heads <= 0)
+        return fail(KDA_ERR_INVALID_ARG, "invalid sizes");
+    // scratch layout: [workspace][cu | seq_off | chunk_seq | chunk_tok]
+    const int64_t bound = max_chunks(total_tokens, num_seqs);
+    const size_t ws_need = kda_workspace_size(total_tokens, num_seqs, num_heads);
+    const size_t ws_part = (ws_need + 255) & ~size_t(255);
+    const size_t meta_words = 4 * (align4((size_t)num_seqs + 1) + align4((size_t)bound));
+    const size_t need = ws_part + meta_words * sizeof(int32_t);
+    if (need > (size_t)KDA_NOALLOC_SCRATCH_BYTES)
+        return fail(KDA_ERR_WORKSPACE,
+                    "kda_chunk_fwd_noalloc: these sizes need %zu bytes of scratch, the built-in "
+                    "scratch holds %llu (KDA_NOALLOC_SCRATCH_BYTES)",
+                    need, (unsigned long long)KDA_NOALLOC_SCRATCH_BYTES);
+    void* scratch = nullptr;
+    int rc = noalloc_scratch(&scratch);
+    if (rc != KDA_OK) return rc;
+    rc = common_checks(q, k, v, g_raw, beta_raw, cu_seqlens, cu_seqlens_host, num_seqs,
+                       total_tokens, num_heads, out, lower_bound, state_dtype, scratch,
+                       (size_t)KDA_NOALLOC_SCRATCH_BYTES);
+    if (rc != KDA_OK) return rc;
+    const int64_t plane = (int64_t)num_heads * kD * kD;
+    if (num_seqs > 0) {
+        if (!state_cache || !state_indices || !has_initial_state)
+            return fail(KDA_ERR_INVALID_ARG,
+                        "state_cache, state_indices and has_initial_state are required");
+        if (num_slots < num_seqs)
+            return fail(KDA_ERR_INVALID_ARG, "num_slots %d < num_seqs %d (slots are distinct)",
+                        num_slots, num_seqs);
+        if (state_stride0 < plane)
+            return fail(KDA_ERR_INVALID_ARG,
+                        "state_stride0 %lld is smaller than the slot plane H*V*K = %lld",
+                        (long long)state_stride0, (long long)plane);
+        const size_t elt = state_elt(state_dtype);
+        if (!aligned(state_cache, 16) || ((size_t)state_stride0 * elt) % 16 != 0)
+            return fail(KDA_ERR_UNSUPPORTED,
+                        "state_cache and its slot stride must be 16-byte aligned");
+    }
+    int64_t n_chunks = 0;
+    for (int32_t n = 0; n < num_seqs; ++n)
+        n_chunks += chunks_of((int64_t)cu_seqlens_host[n + 1] - cu_seqlens_host[n]);
+
+    uint8_t* base = static_cast<uint8_t*>(scratch);
+    int32_t* meta = reinterpret_cast<int32_t*>(base + ws_part);
+    int32_t* mcu = meta;
+    int32_t* off = mcu + align4((size_t)num_seqs + 1);
+    int32_t* cseq = off + align4((size_t)num_seqs + 1);
+    int32_t* ctok = cseq + align4((size_t)bound);
+
+    cudaError_t e = cudaMemsetAsync(base, 0, sizeof(int), stream);  // status word
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (status)");
+    if (num_seqs > 0) {
+        kda_noalloc_meta<<<1, 1024, 0, stream>>>(cu_seqlens, num_seqs, kChunk, mcu, off, cseq,
+                                                  ctok);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "chunk table kernel launch");
+    }
+    kda::FwdParams p{};
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k = static_cast<const __nv_bfloat16*>(k);
+    p.v = static_cast<const __nv_bfloat16*>(v);
+    p.g_raw = g_raw;
+    p.beta_raw = beta_raw;
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.H = num_heads;
+    p.N = num_seqs;
+    p.n_chunks = (int)n_chunks;
+    p.T = total_tokens;
+    p.lower_bound = lower_bound;
+    p.cu = mcu;
+    p.seq_off = off;
+    p.chunk_seq = cseq;
+    p.chunk_tok = ctok;
+    p.ws = base + kda::kWsHeader;
+    p.status = reinterpret_cast<int*>(base);
+    p.st_in = state_cache;
+    p.st_out = state_cache;
+    p.st_in_stride = state_stride0;
+    p.st_out_stride = state_stride0;
+    p.st_in_idx = state_indices;
+    p.st_out_idx = state_indices;
+    p.has_init = has_initial_state;
+    p.st_dtype = state_dtype;
+    e = kda::launch_forward(p, stream, nullptr);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return KDA_OK;
+}
