@@ -320,7 +320,7 @@ def load_traffic(kernel, workload):
         with open(path) as f:
             d = json.load(f)
         ent = d[kernel]
-        src = os.path.join(ROOT, "kda_prefill_gb300", "csrc", "kda_kernels.cu")
+        src = os.path.join(ROOT, ent["source"])
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         if ent.get("source_sha") != sha or ent.get("workload") != workload:
             return None
