@@ -21,16 +21,18 @@
 // below 1e-38.  Off-diagonal blocks run as fp16 MMAs (m16n8k16) on those
 // factored operands.  Inside a diagonal block e^{G_i - G_j} = P_i / P_j; with
 // lower_bound >= -5 a block holds at most 80 nats of decay, so P >= e^-80 and
-// 1/P stay in fp32 range, and these blocks run as tf32 MMAs (m16n8k8) for the
-// extra mantissa the near-diagonal entries need.
+// 1/P stay in fp32 range, and these blocks run as tf32 MMAs (m16n8k8) on fp32
+// operand tiles for the extra mantissa the near-diagonal entries need.
 //
 // The solve is a blocked forward substitution on the right-hand sides:
 // W_I = T_II (X_I - sum_{J<I} A_IJ W_J) with the 16x16 inverses T_II computed in
 // registers; each warp owns 16 of the 256 columns of [X | Y].
 //
 // Data movement: inputs by TMA tiled loads (3-D tensor maps over [T][H][128],
-// 128-byte swizzle), double-buffered one item ahead; outputs are staged in
-// shared memory in their workspace layout and written by TMA bulk stores.
+// 128-byte swizzle); the next item's q, k, g are loaded as soon as the decay
+// pass has consumed the current ones, v one item ahead.  qg and kg go out as
+// 16-byte stores, w, u and A_qk are staged in shared memory in their
+// workspace layout and written by TMA bulk stores.
 
 #include <cuda.h>
 
@@ -48,24 +50,25 @@ using namespace dev;
 constexpr int C = kC;
 constexpr int kThreads = 512;
 
-// Shared-memory layout (bytes).  Stage s holds q, k (bf16 [64][128], swizzled
-// halves) and g (fp32 [64][128], swizzled quarters) of one item.
-constexpr int kStageBytes = 65536;
-constexpr int kQ = 0, kK = 16384, kG = 32768;
-constexpr int kV = 131072;       // v bf16 [64][128] -> b v fp16 -> u (in place)
-constexpr int kInvP = 147456;    // 1/P fp32 [64][128]; then the qg, kg tiles (fp16) to store
-constexpr int kLQ = 180224;      // q^ P fp16, rows 16..63 ([48][128])
-constexpr int kLK = 192512;      // k^ P fp16, rows 16..63
-constexpr int kRO = 204800;      // k^ E_B/P fp16, rows 0..47
-constexpr int kSc = 217088;      // rq[64] rk[64] beta[64] | EB, F1, F2 [4][128] (fp32)
+// Shared-memory layout (bytes).
+constexpr int kQ = 0;          // q bf16 [64][128] (TMA, swizzled halves)
+constexpr int kK = 16384;      // k bf16
+constexpr int kG = 32768;      // g_raw fp32 [64][128] (TMA, swizzled quarters)
+constexpr int kV = 65536;      // v bf16 -> b v fp16 -> u (in place)
+constexpr int kLq32 = 81920;   // q^ P fp32 [64][128]; later u for the store ([8][64][16])
+constexpr int kLk32 = 114688;  // k^ P fp32 [64][128]
+constexpr int kRd32 = 147456;  // k^ / P fp32 [64][128]; later A_qk, -A_kk, A_kk diag, T_II
+constexpr int kLQ = 180224;    // q^ P fp16, rows 16..63 ([48][128]); later X -> w ([64][128])
+constexpr int kLK = 192512;    // k^ P fp16, rows 16..63 ([48][128])
+constexpr int kRO = 204800;    // k^ E_B/P fp16, rows 0..63 ([64][128])
+constexpr int kSc = 221184;    // rq[64] rk[64] beta[64] | EB, F1, F2 [4][128] (fp32)
 constexpr int kBar = kSc + 768 + 3 * 2048;
 constexpr int kSmemBytes = kBar + 64;
-// After the A-tile MMAs the LQ/LK/RO area holds the solve operands and A_qk:
-constexpr int kNAk = kLQ;               // -A_kk off-diagonal blocks, fp16 [64][64] (8 KB)
-constexpr int kAkd = kLQ + 8192;        // A_kk diagonal blocks, fp32 [4][16][16] (4 KB)
-constexpr int kT16 = kLQ + 12288;       // T_II diagonal blocks, fp16 [64][64] tile (8 KB)
-constexpr int kAqkStage = kLQ + 20480;  // A_qk, fp16 [64][64] tile (8 KB), to store
-// The P area of the current stage finally holds u ([8][64][16] fp16) to store.
+// Reuse of the k^/P area after the tile MMAs:
+constexpr int kAqkStage = kRd32;          // A_qk fp16 [64][64] tile, to store (8 KB)
+constexpr int kNAk = kRd32 + 8192;        // -A_kk off-diagonal blocks, fp16 [64][64] (8 KB)
+constexpr int kAkd = kRd32 + 16384;       // A_kk diagonal blocks, fp32 [4][16][16] (4 KB)
+constexpr int kT16 = kRd32 + 20480;       // T_II diagonal blocks, fp16 [64][64] tile (8 KB)
 
 struct IntraMaps {
     CUtensorMap q, k, v, g;
@@ -89,12 +92,13 @@ __device__ __forceinline__ float sumsq_bf16x8(const uint4 v) {
     return s;
 }
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float* o) {
+__device__ __forceinline__ void half8_to_f32(const uint4 v, float* o) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        o[2 * i] = __uint_as_float(w[i] << 16);
-        o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+        o[2 * i] = f.x;
+        o[2 * i + 1] = f.y;
     }
 }
 
@@ -113,6 +117,12 @@ __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Off-diagonal block pairs in order (1,0) (2,0) (2,1) (3,0) (3,1) (3,2).
+__device__ __forceinline__ void pair_of(int pi, int& I, int& J) {
+    I = pi < 1 ? 1 : (pi < 3 ? 2 : 3);
+    J = pi - I * (I - 1) / 2;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -121,8 +131,8 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
     float* beta = rk + 64;
     float* EB = beta + 64;  // [4][128] decay total of each 16-row block
     float* F1 = EB + 512;   // [4][128] decay of the blocks before B (e^G at the block start)
-    float* F2 = F1 + 512;   // [4][128] E_B times the decay of the blocks after B
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBar);  // [0,1] inputs, [2] v
+    float* F2 = F1 + 512;   // [4][128] decay of the blocks after B
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBar);  // [0] q,k,g  [1] v
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -139,7 +149,6 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
     if (tid == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
-        mbar_init(&bar[2], 1);
         fence_mbar_init();
         prefetch_tmap(&maps.q);
         prefetch_tmap(&maps.k);
@@ -149,23 +158,22 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
     __syncthreads();
 
     // TMA issue (thread 0).
-    auto issue_inputs = [&](int it, int stage) {
-        uint8_t* st = smem + stage * kStageBytes;
+    auto issue_inputs = [&](int it) {
         const int t0 = p.chunk_tok[it / H], h = it % H;
-        mbar_arrive_expect_tx(&bar[stage], 65536);
-        tma_load_3d(st + kQ, &maps.q, &bar[stage], 0, h, t0);
-        tma_load_3d(st + kQ + 8192, &maps.q, &bar[stage], 64, h, t0);
-        tma_load_3d(st + kK, &maps.k, &bar[stage], 0, h, t0);
-        tma_load_3d(st + kK + 8192, &maps.k, &bar[stage], 64, h, t0);
+        mbar_arrive_expect_tx(&bar[0], 65536);
+        tma_load_3d(smem + kQ, &maps.q, &bar[0], 0, h, t0);
+        tma_load_3d(smem + kQ + 8192, &maps.q, &bar[0], 64, h, t0);
+        tma_load_3d(smem + kK, &maps.k, &bar[0], 0, h, t0);
+        tma_load_3d(smem + kK + 8192, &maps.k, &bar[0], 64, h, t0);
 #pragma unroll
         for (int qt = 0; qt < 4; ++qt)
-            tma_load_3d(st + kG + qt * 8192, &maps.g, &bar[stage], 32 * qt, h, t0);
+            tma_load_3d(smem + kG + qt * 8192, &maps.g, &bar[0], 32 * qt, h, t0);
     };
     auto issue_v = [&](int it) {
         const int t0 = p.chunk_tok[it / H], h = it % H;
-        mbar_arrive_expect_tx(&bar[2], 16384);
-        tma_load_3d(smem + kV, &maps.v, &bar[2], 0, h, t0);
-        tma_load_3d(smem + kV + 8192, &maps.v, &bar[2], 64, h, t0);
+        mbar_arrive_expect_tx(&bar[1], 16384);
+        tma_load_3d(smem + kV, &maps.v, &bar[1], 0, h, t0);
+        tma_load_3d(smem + kV + 8192, &maps.v, &bar[1], 64, h, t0);
     };
     auto load_braw = [&](int it) -> float {
         const int ch = it / H, hh = it % H;
@@ -175,30 +183,25 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
     };
 
     const int first = blockIdx.x;
-    if (tid == 0 && first < n_items) issue_inputs(first, 0);
+    if (tid == 0 && first < n_items) {
+        issue_inputs(first);
+        issue_v(first);
+    }
     float braw_next = (tid < C && first < n_items) ? load_braw(first) : 0.f;
 
     int n_local = 0;
     for (int it = first; it < n_items; it += gridDim.x, ++n_local) {
-        const int stage = n_local & 1;
-        const int chunk = it / H, h = it % H;
+        const int chunk = it / H;
         const int tok0 = p.chunk_tok[chunk];
         const int seq = p.chunk_seq[chunk];
         const int len = min(C, p.cu[seq + 1] - tok0);
-        uint8_t* st = smem + stage * kStageBytes;
         uint8_t* blk = p.ws + (size_t)it * kWsBytes;
         const int nxt = it + gridDim.x;
-        (void)h;
 
-        if (tid == 0) {
-            bulk_wait_read_all();  // the previous item's stores have read their staging
-            issue_v(it);
-            if (nxt < n_items) issue_inputs(nxt, stage ^ 1);
-        }
         const float braw = braw_next;
         if (tid < C && nxt < n_items) braw_next = load_braw(nxt);
 
-        const bool ok_in = mbar_wait(&bar[stage], (n_local >> 1) & 1);
+        const bool ok_in = mbar_wait(&bar[0], n_local & 1);
         if (__syncthreads_or(!ok_in)) {
             if (tid == 0 && p.status) atomicOr(p.status, 1);
             break;
@@ -212,8 +215,8 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int c = 16 * cg + 8 * j;
-                sq += sumsq_bf16x8(*reinterpret_cast<const uint4*>(st + kQ + sw128_off(r, c, 64)));
-                sk += sumsq_bf16x8(*reinterpret_cast<const uint4*>(st + kK + sw128_off(r, c, 64)));
+                sq += sumsq_bf16x8(*reinterpret_cast<const uint4*>(smem + kQ + sw128_off(r, c, 64)));
+                sk += sumsq_bf16x8(*reinterpret_cast<const uint4*>(smem + kK + sw128_off(r, c, 64)));
             }
 #pragma unroll
             for (int o = 4; o < 32; o <<= 1) {
@@ -226,13 +229,17 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
                 rk[r] = valid ? rsqrtf(sk + 1e-6f) : 0.f;
             }
             if (tid < C) beta[tid] = (tid < len) ? __fdividef(1.f, 1.f + __expf(-braw)) : 0.f;
+            // the previous item's bulk stores must have read the staging areas
+            // (u in the q^P area, A_qk in the k^/P area, w in the LQ area) before
+            // this item's decay pass rewrites them
+            if (tid == 0) bulk_wait_read_all();
         }
         __syncthreads();
 
-        // ---- decay products per (16-row block, channel) -----------------------
-        //   forward: a = e^{lb sigmoid(g)}, P (in place of g), q^ P and k^ P (left
-        //   operands); backward: R = P_end / P (suffix product), 1/P = R / P_end,
-        //   k^ R (right operand of the off-diagonal blocks).
+        // ---- decay pass per (16-row block, channel) ---------------------------
+        //   forward: a = e^{lb sigmoid(g)}, P; q^ P and k^ P (fp32 for the diagonal
+        //   tiles, fp16 for the off-diagonal left operands); backward: R = P_end/P
+        //   (suffix product), k^ / P = k^ R / P_end (fp32) and k^ R (fp16).
         {
             const int B = tid >> 7, c = tid & 127;
             float P = 1.f;
@@ -240,18 +247,19 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int r = 16 * B + i;
-                float* gp = reinterpret_cast<float*>(st + kG + sw128f_off(r, c, 64));
-                const float sg = __fdividef(1.f, 1.f + __expf(-*gp));
+                const uint32_t o32 = sw128f_off(r, c, 64);
+                const float gr = *reinterpret_cast<const float*>(smem + kG + o32);
+                const float sg = __fdividef(1.f, 1.f + __expf(-gr));
                 a[i] = (r < len) ? __expf(lb * sg) : 1.f;
                 P *= a[i];
-                *gp = P;
-                const float qh = bf(st + kQ, r, c) * rq[r];
-                kh[i] = bf(st + kK, r, c) * rk[r];
+                const float qh = bf(smem + kQ, r, c) * rq[r];
+                kh[i] = bf(smem + kK, r, c) * rk[r];
+                *reinterpret_cast<float*>(smem + kLq32 + o32) = qh * P;
+                *reinterpret_cast<float*>(smem + kLk32 + o32) = kh[i] * P;
                 if (B >= 1) {
-                    *reinterpret_cast<__half*>(smem + kLQ + sw128_off(r - 16, c, 48)) =
-                        __float2half_rn(qh * P);
-                    *reinterpret_cast<__half*>(smem + kLK + sw128_off(r - 16, c, 48)) =
-                        __float2half_rn(kh[i] * P);
+                    const uint32_t o16 = sw128_off(r - 16, c, 48);
+                    *reinterpret_cast<__half*>(smem + kLQ + o16) = __float2half_rn(qh * P);
+                    *reinterpret_cast<__half*>(smem + kLK + o16) = __float2half_rn(kh[i] * P);
                 }
             }
             EB[B * 128 + c] = P;
@@ -260,65 +268,53 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
 #pragma unroll
             for (int i = 15; i >= 0; --i) {
                 const int r = 16 * B + i;
-                *reinterpret_cast<float*>(smem + kInvP + sw128f_off(r, c, 64)) = R * inv_end;
-                if (B <= 2)
-                    *reinterpret_cast<__half*>(smem + kRO + sw128_off(r, c, 48)) =
-                        __float2half_rn(kh[i] * R);
+                *reinterpret_cast<float*>(smem + kRd32 + sw128f_off(r, c, 64)) = kh[i] * R * inv_end;
+                *reinterpret_cast<__half*>(smem + kRO + sw128_off(r, c, 64)) = __float2half_rn(kh[i] * R);
                 R *= a[i];
             }
         }
         __syncthreads();
+        // q, k, g of this item are consumed: load the next item's now
+        if (tid == 0 && nxt < n_items) issue_inputs(nxt);
 
-        // ---- A tiles (warps 0-7), overlapped with the qg/kg/X pass (warps 8-15) ----
-        float accD[2][2][4] = {};  // diagonal warps: [q/k][nt][e]
-        float accO[3][2][4] = {};  // off-diagonal warps: three block pairs
-        uint32_t xo[2][3][8];      // X-pass warps: [pass][qg/kg/X][half2 pairs]
-        if (warp < 4) {
-            // diagonal block I = warp, tf32 (m16n8k8) on P-factored operands
-            const int I = warp;
+        // ---- A tiles: diagonal blocks (warps 0-7, tf32), off-diagonal pairs
+        //      (warps 8-15, fp16), block decay factors (warps 12-15) -------------
+        float accD[2][4] = {};     // diagonal: [nt][e]
+        float accO[2][2][4] = {};  // off-diagonal: up to two items
+        if (warp < 8) {
+            const int I = warp >> 1, which = warp & 1;  // which: 0 = q-left (A_qk), 1 = k-left
+            const uint8_t* L = smem + (which ? kLk32 : kLq32);
             const int r0 = 16 * I + g8, r1 = r0 + 8;
-            const float rq0 = rq[r0], rq1 = rq[r1], rk0 = rk[r0], rk1 = rk[r1];
 #pragma unroll 4
             for (int ks = 0; ks < 16; ++ks) {
                 const int cl = 8 * ks + tq, ch = cl + 4;
-                const float P00 = f32t(st + kG, r0, cl), P10 = f32t(st + kG, r1, cl);
-                const float P01 = f32t(st + kG, r0, ch), P11 = f32t(st + kG, r1, ch);
-                uint32_t aq[4], ak[4], b[2][2];
-                aq[0] = to_tf32(bf(st + kQ, r0, cl) * rq0 * P00);
-                aq[1] = to_tf32(bf(st + kQ, r1, cl) * rq1 * P10);
-                aq[2] = to_tf32(bf(st + kQ, r0, ch) * rq0 * P01);
-                aq[3] = to_tf32(bf(st + kQ, r1, ch) * rq1 * P11);
-                ak[0] = to_tf32(bf(st + kK, r0, cl) * rk0 * P00);
-                ak[1] = to_tf32(bf(st + kK, r1, cl) * rk1 * P10);
-                ak[2] = to_tf32(bf(st + kK, r0, ch) * rk0 * P01);
-                ak[3] = to_tf32(bf(st + kK, r1, ch) * rk1 * P11);
-                // B columns j = rows r0 (n-tile 0) and r1 (n-tile 1): k^_j / P_j
-                b[0][0] = to_tf32(bf(st + kK, r0, cl) * rk0 * f32t(smem + kInvP, r0, cl));
-                b[0][1] = to_tf32(bf(st + kK, r0, ch) * rk0 * f32t(smem + kInvP, r0, ch));
-                b[1][0] = to_tf32(bf(st + kK, r1, cl) * rk1 * f32t(smem + kInvP, r1, cl));
-                b[1][1] = to_tf32(bf(st + kK, r1, ch) * rk1 * f32t(smem + kInvP, r1, ch));
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    mma_tf32(accD[0][nt], aq, b[nt][0], b[nt][1]);
-                    mma_tf32(accD[1][nt], ak, b[nt][0], b[nt][1]);
-                }
+                uint32_t a4[4], b[2][2];
+                a4[0] = to_tf32(f32t(L, r0, cl));
+                a4[1] = to_tf32(f32t(L, r1, cl));
+                a4[2] = to_tf32(f32t(L, r0, ch));
+                a4[3] = to_tf32(f32t(L, r1, ch));
+                b[0][0] = to_tf32(f32t(smem + kRd32, r0, cl));
+                b[0][1] = to_tf32(f32t(smem + kRd32, r0, ch));
+                b[1][0] = to_tf32(f32t(smem + kRd32, r1, cl));
+                b[1][1] = to_tf32(f32t(smem + kRd32, r1, ch));
+                mma_tf32(accD[0], a4, b[0][0], b[0][1]);
+                mma_tf32(accD[1], a4, b[1][0], b[1][1]);
             }
-        } else if (warp < 8) {
-            // off-diagonal block pairs, fp16 (m16n8k16) on bounded operands;
-            // items in order (1,0) (2,0) (2,1) (3,0) (3,1) (3,2), q-left then k-left
+        } else {
             const uint32_t rt = smem_u32(smem + kRO);
+            const int n_my = (warp < 12) ? 2 : 1;
 #pragma unroll
-            for (int q3 = 0; q3 < 3; ++q3) {
-                const int itm = (warp - 4) * 3 + q3;
-                const int pi = itm >> 1, which = itm & 1;
-                const int tI = pi < 1 ? 1 : (pi < 3 ? 2 : 3);
-                const int tJ = pi - tI * (tI - 1) / 2;
+            for (int q2 = 0; q2 < 2; ++q2) {
+                if (q2 >= n_my) break;
+                const int itm = (warp - 8) + 8 * q2;  // warps 8-11: items w-8, w; 12-15: w-8
+                const int which = itm & 1;
+                int tI, tJ;
+                pair_of(itm >> 1, tI, tJ);
                 const uint32_t lt = smem_u32(smem + (which ? kLK : kLQ));
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     uint32_t a4[4], b4[4];
-                    ldsm_x4(lt + sw128_off(16 * (tI - 1) + rr + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1),
-                                           48),
+                    ldsm_x4(lt + sw128_off(16 * (tI - 1) + rr + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1), 48),
                             a4[0], a4[1], a4[2], a4[3]);
                     if (tI - tJ >= 2) {
                         const int cc = 16 * ks + 2 * tq;
@@ -337,97 +333,33 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
                         ah[2] = __hmul2(ah[2], mhi);
                         ah[3] = __hmul2(ah[3], mhi);
                     }
-                    ldsm_x4(rt + sw128_off(16 * tJ + rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1), 48),
+                    ldsm_x4(rt + sw128_off(16 * tJ + rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1), 64),
                             b4[0], b4[1], b4[2], b4[3]);
-                    mma_f16(accO[q3][0], a4, b4[0], b4[1]);
-                    mma_f16(accO[q3][1], a4, b4[2], b4[3]);
+                    mma_f16(accO[q2][0], a4, b4[0], b4[1]);
+                    mma_f16(accO[q2][1], a4, b4[2], b4[3]);
                 }
             }
-        } else {
-            // block-level decay factors and gamma, then qg, kg, X into registers
-            const int t2 = tid - 256;
-            for (int e = t2; e < 512; e += 256) {
-                const int Bq = e >> 7, cq = e & 127;
-                float pre = 1.f, suf = 1.f;
+            if (warp >= 12) {
+                // F1, F2 and gamma = e^{G_C}
+                for (int e = tid - 384; e < 512; e += 128) {
+                    const int Bq = e >> 7, cq = e & 127;
+                    float pre = 1.f, suf = 1.f;
 #pragma unroll
-                for (int Bm = 0; Bm < 4; ++Bm) {
-                    const float x = EB[Bm * 128 + cq];
-                    if (Bm < Bq) pre *= x;
-                    if (Bm > Bq) suf *= x;
-                }
-                F1[e] = pre;
-                F2[e] = EB[e] * suf;
-                if (Bq == 0) reinterpret_cast<float*>(blk + kWsGammaOff)[cq] = EB[e] * suf;
-            }
-            asm volatile("bar.sync 2, 256;" ::: "memory");
-            const int r = (lane & 7) + 8 * (t2 >> 5);  // 8 consecutive lanes: 8 rows
-            const int cg = lane >> 3;                   // 32-channel group
-            const int Br = r >> 4;
-            const float qs = rq[r], ksc = rk[r], bt = beta[r];
-#pragma unroll
-            for (int pass = 0; pass < 2; ++pass) {
-                const int c0 = 32 * cg + 16 * pass;
-                float Pv[16], Iv[16], qv[16], kv[16];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    *reinterpret_cast<float4*>(Pv + 4 * j) =
-                        *reinterpret_cast<const float4*>(st + kG + sw128f_off(r, c0 + 4 * j, 64));
-                    *reinterpret_cast<float4*>(Iv + 4 * j) =
-                        *reinterpret_cast<const float4*>(smem + kInvP + sw128f_off(r, c0 + 4 * j, 64));
-                }
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    bf16x8_to_f32(*reinterpret_cast<const uint4*>(st + kQ + sw128_off(r, c0 + 8 * j, 64)),
-                                  qv + 8 * j);
-                    bf16x8_to_f32(*reinterpret_cast<const uint4*>(st + kK + sw128_off(r, c0 + 8 * j, 64)),
-                                  kv + 8 * j);
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    float o[3][2];
-#pragma unroll
-                    for (int e2 = 0; e2 < 2; ++e2) {
-                        const int e = 2 * j + e2;
-                        const float f1 = F1[Br * 128 + c0 + e], f2 = F2[Br * 128 + c0 + e];
-                        const float qh = qv[e] * qs, kh = kv[e] * ksc;
-                        const float eG = f1 * Pv[e];
-                        o[0][e2] = qh * eG;             // qg
-                        o[1][e2] = kh * Iv[e] * f2;     // kg
-                        o[2][e2] = bt * kh * eG;        // X
+                    for (int Bm = 0; Bm < 4; ++Bm) {
+                        const float x = EB[Bm * 128 + cq];
+                        if (Bm < Bq) pre *= x;
+                        if (Bm > Bq) suf *= x;
                     }
-                    xo[pass][0][j] = pack_half2(o[0][0], o[0][1]);
-                    xo[pass][1][j] = pack_half2(o[1][0], o[1][1]);
-                    xo[pass][2][j] = pack_half2(o[2][0], o[2][1]);
+                    F1[e] = pre;
+                    F2[e] = suf;
+                    if (Bq == 0) reinterpret_cast<float*>(blk + kWsGammaOff)[cq] = EB[e] * suf;
                 }
             }
         }
-        __syncthreads();  // every read of q, k, P, 1/P and the LQ/LK/RO operands is done
+        __syncthreads();  // the fp32 and fp16 operand tiles are consumed
 
-        // ---- stage qg, kg (in the 1/P area), X (in place of q), A tiles ---------
-        if (warp >= 8) {
-            const int t2 = tid - 256;
-            const int r = (lane & 7) + 8 * (t2 >> 5);
-            const int cg = lane >> 3;
-#pragma unroll
-            for (int pass = 0; pass < 2; ++pass) {
-                const int c0 = 32 * cg + 16 * pass;
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const uint32_t o = sw128_off(r, c0 + 8 * j, 64);
-                    *reinterpret_cast<uint4*>(smem + kInvP + o) =
-                        make_uint4(xo[pass][0][4 * j], xo[pass][0][4 * j + 1], xo[pass][0][4 * j + 2],
-                                   xo[pass][0][4 * j + 3]);
-                    *reinterpret_cast<uint4*>(smem + kInvP + 16384 + o) =
-                        make_uint4(xo[pass][1][4 * j], xo[pass][1][4 * j + 1], xo[pass][1][4 * j + 2],
-                                   xo[pass][1][4 * j + 3]);
-                    *reinterpret_cast<uint4*>(st + kQ + o) =
-                        make_uint4(xo[pass][2][4 * j], xo[pass][2][4 * j + 1], xo[pass][2][4 * j + 2],
-                                   xo[pass][2][4 * j + 3]);
-                }
-            }
-        } else {
-            // A_qk (j <= i) -> staging tile; A_kk (j < i, times beta_i): diagonal
-            // blocks fp32, off-diagonal blocks negated fp16.
+        // ---- A_qk / A_kk into place, and the qg / kg / X pass -----------------
+        {
             auto put = [&](int sel, int tI, int tJ, const float (&acc)[2][4]) {
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
@@ -436,43 +368,75 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
                         const int i = 16 * tI + g8 + 8 * hh;
                         const int j = 16 * tJ + 8 * nt + 2 * tq;
                         float x0 = acc[nt][2 * hh], x1 = acc[nt][2 * hh + 1];
-                        if (sel == 0) {
+                        if (sel == 0) {  // A_qk, j <= i
                             if (tI == tJ) {
                                 if (j > i) x0 = 0.f;
                                 if (j + 1 > i) x1 = 0.f;
                             }
                             *reinterpret_cast<uint32_t*>(smem + kAqkStage + sw64_off(i, j)) =
                                 pack_half2(x0, x1);
-                        } else if (tI == tJ) {
+                        } else if (tI == tJ) {  // A_kk diagonal block, fp32, j < i
                             float* d = reinterpret_cast<float*>(smem + kAkd) + tI * 256;
                             const float bi = beta[i];
                             d[(i & 15) * 16 + (j & 15)] = (j >= i) ? 0.f : bi * x0;
                             d[(i & 15) * 16 + (j & 15) + 1] = (j + 1 >= i) ? 0.f : bi * x1;
-                        } else {
+                        } else {  // -A_kk off-diagonal block, fp16
                             const float bi = -beta[i];
                             *reinterpret_cast<uint32_t*>(smem + kNAk + sw64_off(i, j)) =
                                 pack_half2(bi * x0, bi * x1);
                         }
                     }
             };
-            if (warp < 4) {
-                put(0, warp, warp, accD[0]);
-                put(1, warp, warp, accD[1]);
+            if (warp < 8) {
+                put(warp & 1, warp >> 1, warp >> 1, accD);
             } else {
-#pragma unroll
-                for (int q3 = 0; q3 < 3; ++q3) {
-                    const int itm = (warp - 4) * 3 + q3;
-                    const int pi = itm >> 1, which = itm & 1;
-                    const int tI = pi < 1 ? 1 : (pi < 3 ? 2 : 3);
-                    const int tJ = pi - tI * (tI - 1) / 2;
-                    put(which, tI, tJ, accO[q3]);
+                const int n_my = (warp < 12) ? 2 : 1;
+                for (int q2 = 0; q2 < n_my; ++q2) {
+                    const int itm = (warp - 8) + 8 * q2;
+                    int tI, tJ;
+                    pair_of(itm >> 1, tI, tJ);
+                    put(itm & 1, tI, tJ, accO[q2]);
                 }
+            }
+            // qg, kg (16-byte stores to the workspace) and X = b k^ e^G (shared)
+            const int r = (lane & 7) + 8 * (warp & 7);
+            const int cg = (lane >> 3) + 4 * (warp >> 3);  // 16-channel group
+            const int c0 = 16 * cg;
+            const int Br = r >> 4;
+            const float bt = beta[r];
+            float lq[16], lk[16], ro[16];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                *reinterpret_cast<float4*>(lq + 4 * j) =
+                    *reinterpret_cast<const float4*>(smem + kLq32 + sw128f_off(r, c0 + 4 * j, 64));
+                *reinterpret_cast<float4*>(lk + 4 * j) =
+                    *reinterpret_cast<const float4*>(smem + kLk32 + sw128f_off(r, c0 + 4 * j, 64));
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                half8_to_f32(*reinterpret_cast<const uint4*>(smem + kRO + sw128_off(r, c0 + 8 * j, 64)),
+                             ro + 8 * j);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                uint32_t oq[4], ok[4], ox[4];
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2) {
+                    const int e = 8 * j + 2 * e2;
+                    const float f1a = F1[Br * 128 + c0 + e], f1b = F1[Br * 128 + c0 + e + 1];
+                    const float f2a = F2[Br * 128 + c0 + e], f2b = F2[Br * 128 + c0 + e + 1];
+                    oq[e2] = pack_half2(lq[e] * f1a, lq[e + 1] * f1b);
+                    ok[e2] = pack_half2(ro[e] * f2a, ro[e + 1] * f2b);
+                    ox[e2] = pack_half2(bt * lk[e] * f1a, bt * lk[e + 1] * f1b);
+                }
+                const uint32_t o = sw128_off(r, c0 + 8 * j, 64);
+                *reinterpret_cast<uint4*>(blk + kWsQGOff + o) = make_uint4(oq[0], oq[1], oq[2], oq[3]);
+                *reinterpret_cast<uint4*>(blk + kWsKGOff + o) = make_uint4(ok[0], ok[1], ok[2], ok[3]);
+                *reinterpret_cast<uint4*>(smem + kLQ + o) = make_uint4(ox[0], ox[1], ox[2], ox[3]);
             }
         }
         fence_proxy_async();
         __syncthreads();
         if (tid == 0) {
-            bulk_s2g(blk + kWsQGOff, smem + kInvP, 32768);  // qg and kg are adjacent
             bulk_s2g(blk + kWsAqkOff, smem + kAqkStage, 8192);
             bulk_commit();
         }
@@ -495,7 +459,7 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
                 *reinterpret_cast<__half*>(smem + kT16 + sw64_off(16 * I + i, 16 * I + col)) =
                     __float2half_rn(t[i]);
         } else {
-            const bool ok_v = mbar_wait(&bar[2], n_local & 1);
+            const bool ok_v = mbar_wait(&bar[1], n_local & 1);
             if (!ok_v && p.status) atomicOr(p.status, 1);
             for (int e = tid - 64; e < C * 64; e += kThreads - 64) {  // pairs of elements
                 const int r = e >> 6, c2 = (e & 63) * 2;
@@ -513,10 +477,10 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
         {
             const bool isu = warp >= 8;
             const int n0 = 16 * (warp & 7);
-            uint8_t* xt = isu ? smem + kV : st + kQ;
+            uint8_t* xt = isu ? smem + kV : smem + kLQ;
             const uint32_t xb = smem_u32(xt);
             const uint32_t nak = smem_u32(smem + kNAk), t16 = smem_u32(smem + kT16);
-            uint8_t* ustage = st + kG + (warp & 7) * kWsUSliceBytes;  // [64][16] fp16
+            uint8_t* ustage = smem + kLq32 + (warp & 7) * kWsUSliceBytes;  // [64][16] fp16
 #pragma unroll
             for (int I = 0; I < 4; ++I) {
                 float acc[2][4];
@@ -576,9 +540,10 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
         fence_proxy_async();
         __syncthreads();
         if (tid == 0) {
-            bulk_s2g(blk + kWsWOff, st + kQ, 16384);
-            bulk_s2g(blk + kWsUOff, st + kG, 16384);
+            bulk_s2g(blk + kWsWOff, smem + kLQ, 16384);
+            bulk_s2g(blk + kWsUOff, smem + kLq32, 16384);
             bulk_commit();
+            if (nxt < n_items) issue_v(nxt);  // v of this item is consumed
         }
     }
     if (tid == 0) bulk_wait_all();  // stores complete before the CTA releases its smem

@@ -1,27 +1,29 @@
-// State scan of the chunkwise KDA forward: one CTA per (sequence, head, group
-// of 16*NG value rows of the state), walking the sequence's chunks in order.
+// State scan of the chunkwise KDA forward: one CTA per (sequence, head, block of
+// VS = 8*NT value rows of the state), walking the sequence's chunks in order.
 //
-// Per chunk, with the incoming state S (V rows x K, fp32 in registers):
-//   U = u - w S^T                 (C x Vs)   new values of the chunk
-//   o = qg S^T + A_qk U           (C x Vs)   written to `out`
-//   S = S Diag(gamma) + U^T kg    (Vs x K)
+// Per chunk, with the incoming state S (VS rows x K):
+//   U = u - w S^T                 (C x VS)   new values of the chunk
+//   S = S Diag(gamma) + U^T kg    (VS x K)   the state after the chunk
+//   o = qg S^T + A_qk U           (C x VS)   written to `out`
 // (ROCm/aiter PR #4741, "Summary": the state scan and the output matmul of the
 // KDA block; "Optimizations Applied": the serial state walk split over value
 // channels.  The pool row is loaded at the start and the final state written
 // back to the same row: ROCm/aiter PR #5754, "Technical Details".)
 //
-// The products are warp-level tensor-core MMAs (m16n8k16, fp16 operands, fp32
-// accumulation).  They are tiny (M = 64, N = 16 per group) and sit on the serial
-// critical path, so operands stay in registers / shared memory between the two
-// dependent products of a chunk.  The chunk's intermediates (w, qg, kg, A_qk,
-// gamma and the group's u columns) arrive by TMA bulk copies into a
-// double-buffered shared-memory stage, one chunk ahead.
-//
-// Warp layout: 4 warps per group of 16 value rows.  Warp wr of a group owns
-// rows 16*wr.. of U and o, and key channels 32*wr.. of S^T (its fp32 master
-// copy lives in that warp's registers).  One extra warp only issues the TMA
-// copies (full/empty mbarrier pair per stage), so no compute warp spends time
-// issuing copies on the serial path.
+// Only the first two products are on the serial path from one chunk to the
+// next, so the CTA is split by role:
+//   * 4 state warps keep S (fp32 master copy in registers, warp wr owning key
+//     channels 32wr..32wr+31 of S^T), compute U and the update, and publish the
+//     chunk's incoming S and its U (fp16) in a two-slot ring;
+//   * 4 output warps compute o from the ring one step behind (warp wr: chunk
+//     rows 16wr..16wr+15) and store it;
+//   * 1 producer warp streams each chunk's intermediates (w, qg, kg, A_qk,
+//     gamma and the CTA's u columns) by TMA bulk copies into a double-buffered
+//     stage.
+// Hand-offs use mbarriers (stage full/empty, ring ready/free); the state warps
+// synchronise among themselves on a named barrier.  Products are warp-level
+// tensor-core MMAs (m16n8k16, fp16 operands, fp32 accumulation); fp16 tiles
+// are written with stmatrix (transposing) and read with ldmatrix.
 
 #include "kda_device.cuh"
 #include "kda_internal.h"
@@ -34,17 +36,25 @@ using namespace dev;
 constexpr int C = kC;
 constexpr int D = kD;
 
-template <int NG>
+constexpr int round1k(int x) { return (x + 1023) / 1024 * 1024; }
+
+template <int NT>
 struct ScanSmem {
-    static constexpr int kShared = kWsSharedBytes;                   // w, qg, kg, aqk, gamma
-    static constexpr int kSharedPad = (kShared + 1023) / 1024 * 1024;
-    static constexpr int kU = NG * kWsUSliceBytes;                   // NG u slices
-    static constexpr int kStage = kSharedPad + (kU + 1023) / 1024 * 1024;
-    static constexpr int kS16 = 2 * kStage;                          // NG x [16][128] fp16
-    static constexpr int kUt = kS16 + NG * 4096;                     // NG x [16][64] fp16
-    static constexpr int kBar = kUt + NG * 2048;                     // full[2], empty[2]
-    static constexpr int kTotal = kBar + 64;
+    static constexpr int VS = 8 * NT;                        // value rows per CTA
+    static constexpr int kShared = kWsSharedBytes;           // w, qg, kg, aqk, gamma
+    static constexpr int kSharedPad = round1k(kShared);
+    static constexpr int kU = (VS / 16) * kWsUSliceBytes;    // the CTA's u columns
+    static constexpr int kStage = kSharedPad + round1k(kU);
+    static constexpr int kS16 = 2 * kStage;                  // 2 slots x [VS][128] fp16
+    static constexpr int kS16Slot = VS * 256;
+    static constexpr int kUt = kS16 + 2 * kS16Slot;          // 2 slots x [VS][64] fp16
+    static constexpr int kUtSlot = VS * 128;
+    static constexpr int kBar = kUt + 2 * kUtSlot;           // mbarriers
+    static constexpr int kTotal = kBar + 128;
 };
+
+constexpr int kStateWarps = 4, kOutWarps = 4;
+constexpr int kThreads = 32 * (kStateWarps + kOutWarps + 1);
 
 __device__ __forceinline__ float load_state(const void* base, int dtype, size_t off) {
     if (dtype == 0) return static_cast<const float*>(base)[off];
@@ -62,21 +72,23 @@ __device__ __forceinline__ void store_state(void* base, int dtype, size_t off, f
     }
 }
 
-template <int NG>
-__global__ void __launch_bounds__(128 * NG + 32, 1) kda_scan_mma(FwdParams p) {
-    using L = ScanSmem<NG>;
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1) kda_scan_mma(FwdParams p) {
+    using L = ScanSmem<NT>;
+    constexpr int VS = L::VS;
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);  // [2]
+    uint64_t* empty = full + 2;                                     // [2]
+    uint64_t* sready = full + 4;                                    // [2]
+    uint64_t* sfree = full + 6;                                     // [2]
 
     const int n = blockIdx.x;
     const int h = blockIdx.y;
-    const int vs0 = blockIdx.z * NG;  // first 16-row value slice of this CTA
+    const int v0 = blockIdx.z * VS;  // first value row of this CTA
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int gi = warp >> 2;   // group
-    const int wr = warp & 3;    // row block / key block within the group
     const int g = lane >> 2, tq = lane & 3;
-    const int mi = lane >> 3, rr = lane & 7;  // ldmatrix addressing
+    const int mi = lane >> 3, rr = lane & 7;  // ldmatrix / stmatrix addressing
 
     const int tok0 = p.cu[n];
     const int len = p.cu[n + 1] - tok0;
@@ -84,210 +96,248 @@ __global__ void __launch_bounds__(128 * NG + 32, 1) kda_scan_mma(FwdParams p) {
     const int nch = p.seq_off[n + 1] - c0;
 
     const uint32_t sm_base = smem_u32(smem);
-    // barrier among the compute warps only (id 1; id 0 is __syncthreads)
-    auto consumer_sync = [&]() {
-        asm volatile("bar.sync 1, %0;" ::"r"(128 * NG) : "memory");
-    };
-    // same barrier, returning whether any compute thread passed `flag` set
-    auto consumer_sync_or = [&](bool flag) -> bool {
-        uint32_t any;
-        asm volatile(
-            "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-            "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-            : "=r"(any)
-            : "r"((uint32_t)flag), "r"(128 * NG)
-            : "memory");
-        return any != 0;
-    };
-    const uint32_t s16 = sm_base + L::kS16 + gi * 4096;  // this group's S (fp16, [16][128])
-    const uint32_t ut = sm_base + L::kUt + gi * 2048;    // this group's U^T (fp16, [16][64])
+    auto stage_base = [&](int s) { return sm_base + s * L::kStage; };
+    auto s16_slot = [&](int b) { return sm_base + L::kS16 + b * L::kS16Slot; };
+    auto ut_slot = [&](int b) { return sm_base + L::kUt + b * L::kUtSlot; };
 
-    constexpr int kConsumerWarps = 4 * NG;
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        mbar_init(&bars[2], kConsumerWarps);
-        mbar_init(&bars[3], kConsumerWarps);
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        mbar_init(&empty[0], kStateWarps + kOutWarps);
+        mbar_init(&empty[1], kStateWarps + kOutWarps);
+        mbar_init(&sready[0], 1);
+        mbar_init(&sready[1], 1);
+        mbar_init(&sfree[0], kOutWarps);
+        mbar_init(&sfree[1], kOutWarps);
         fence_mbar_init();
     }
-    if (warp == kConsumerWarps) {
-        // ---- producer warp: TMA copies of each chunk, one stage ahead ----------
-        __syncthreads();
+    __syncthreads();
+
+    // ======================= producer warp ==================================
+    if (warp == kStateWarps + kOutWarps) {
         if (lane == 0) {
             for (int lc = 0; lc < nch; ++lc) {
                 const int stage = lc & 1;
-                if (lc >= 2 && !mbar_wait(&bars[2 + stage], ((lc >> 1) - 1) & 1)) {
+                if (lc >= 2 && !mbar_wait(&empty[stage], ((lc >> 1) - 1) & 1)) {
                     if (p.status) atomicOr(p.status, 1);
                     break;
                 }
                 const size_t ch = (size_t)(c0 + lc) * p.H + h;
                 const uint8_t* src = p.ws + ch * kWsBytes;
                 uint8_t* dst = smem + stage * L::kStage;
-                mbar_arrive_expect_tx(&bars[stage], (uint32_t)(L::kShared + L::kU));
-                bulk_g2s(dst, src, (uint32_t)L::kShared, &bars[stage]);
-                bulk_g2s(dst + L::kSharedPad, src + kWsUOff + vs0 * kWsUSliceBytes,
-                         (uint32_t)L::kU, &bars[stage]);
+                mbar_arrive_expect_tx(&full[stage], (uint32_t)(L::kShared + L::kU));
+                bulk_g2s(dst, src, (uint32_t)L::kShared, &full[stage]);
+                bulk_g2s(dst + L::kSharedPad, src + kWsUOff + (v0 / 16) * kWsUSliceBytes,
+                         (uint32_t)L::kU, &full[stage]);
             }
         }
         return;
     }
 
-    // ---- initial state -> fp32 master copy in registers --------------------
+    // ======================= output warps ===================================
+    if (warp >= kStateWarps) {
+        const int wr = warp - kStateWarps;  // chunk rows 16wr..16wr+15
+        for (int lc = 0; lc < nch; ++lc) {
+            const int b = lc & 1;
+            const uint32_t par = (lc >> 1) & 1;
+            if (!mbar_wait(&full[b], par) || !mbar_wait(&sready[b], par)) {
+                if (p.status) atomicOr(p.status, 1);
+                break;
+            }
+            const uint32_t st = stage_base(b);
+            const uint32_t tqg = st + kWsQGOff, taqk = st + kWsAqkOff;
+            const uint32_t s16 = s16_slot(b), ut = ut_slot(b);
+            // qg S^T (two accumulation chains over the key halves) + A_qk U
+            float acc[NT][4] = {}, acc2[NT][4] = {};
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                uint32_t a[4];
+                ldsm_x4(tqg + sw128_off(16 * wr + rr + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1), 64),
+                        a[0], a[1], a[2], a[3]);
+                float (*d)[4] = (ks & 1) ? acc2 : acc;
+#pragma unroll
+                for (int np = 0; np < NT / 2; ++np) {
+                    uint32_t bb[4];
+                    ldsm_x4(s16 + sw128_off(16 * np + rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1), VS),
+                            bb[0], bb[1], bb[2], bb[3]);
+                    mma_f16(d[2 * np], a, bb[0], bb[1]);
+                    mma_f16(d[2 * np + 1], a, bb[2], bb[3]);
+                }
+            }
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {  // A_qk lower triangular: key blocks 0..wr
+                if (ks > wr) break;
+                uint32_t a[4];
+                ldsm_x4(taqk + sw64_off(16 * wr + rr + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1)), a[0],
+                        a[1], a[2], a[3]);
+#pragma unroll
+                for (int np = 0; np < NT / 2; ++np) {
+                    uint32_t bb[4];
+                    ldsm_x4(ut + sw64_off(16 * np + rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1)), bb[0],
+                            bb[1], bb[2], bb[3]);
+                    mma_f16(acc2[2 * np], a, bb[0], bb[1]);
+                    mma_f16(acc2[2 * np + 1], a, bb[2], bb[3]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&sfree[b]);
+                mbar_arrive(&empty[b]);
+            }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int i = 16 * wr + g + 8 * hh;
+                if (lc * C + i < len) {
+                    const size_t t = (size_t)(tok0 + lc * C + i);
+                    __nv_bfloat16* orow = p.out + (t * p.H + h) * D + v0;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const uint32_t pv = pack_bf162(acc[nt][2 * hh] + acc2[nt][2 * hh],
+                                                       acc[nt][2 * hh + 1] + acc2[nt][2 * hh + 1]);
+                        *reinterpret_cast<uint32_t*>(orow + 8 * nt + 2 * tq) = pv;
+                    }
+                }
+            }
+        }
+        return;
+    }
+
+    // ======================= state warps ====================================
+    const int wr = warp;  // key channels 32wr..32wr+31 of S^T
+    auto state_sync = [&]() { asm volatile("bar.sync 1, 128;" ::: "memory"); };
+    auto state_sync_or = [&](bool flag) -> bool {
+        uint32_t any;
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+            "bar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(any)
+            : "r"((uint32_t)flag)
+            : "memory");
+        return any != 0;
+    };
+
     const bool has_init = p.has_init ? (p.has_init[n] != 0) : (p.st_in != nullptr);
     const int64_t in_slot = p.st_in_idx ? p.st_in_idx[n] : n;
     const int64_t out_slot = p.st_out_idx ? p.st_out_idx[n] : n;
     const size_t in_base = (size_t)in_slot * p.st_in_stride + (size_t)h * D * D;
     const size_t out_base = (size_t)out_slot * p.st_out_stride + (size_t)h * D * D;
-    const int vcol0 = (vs0 + gi) * 16;  // first value row of this group
 
-    float Sm[2][2][4];  // [mt][nt][e]: k = 32wr+16mt+g+8(e>>1), v = 8nt+2tq+(e&1)
+    float Sm[2][NT][4];  // [mt][nt][e]: k = 32wr+16mt+g+8(e>>1), v = 8nt+2tq+(e&1)
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int kk = 32 * wr + 16 * mt + g + 8 * (e >> 1);
-                const int vv = vcol0 + 8 * nt + 2 * tq + (e & 1);
+                const int vv = v0 + 8 * nt + 2 * tq + (e & 1);
                 Sm[mt][nt][e] =
                     has_init ? load_state(p.st_in, p.st_dtype, in_base + (size_t)vv * D + kk) : 0.f;
             }
 
-    auto write_s16 = [&]() {
+    // S (fp16) into ring slot b: S^T fragments stored transposed as S[v][k].
+    auto write_s16 = [&](int b) {
+        const uint32_t s16 = s16_slot(b);
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+            for (int np = 0; np < NT / 2; ++np) {
+                // matrices (n-tile 2np + (mi >> 1), key half mi & 1): rows v, columns k
+                const int vrow = 16 * np + 8 * (mi >> 1) + rr;
+                const int kcol = 32 * wr + 16 * mt + 8 * (mi & 1);
+                stsm_x4_t(s16 + sw128_off(vrow, kcol, VS),
+                          pack_half2(Sm[mt][2 * np][0], Sm[mt][2 * np][1]),
+                          pack_half2(Sm[mt][2 * np][2], Sm[mt][2 * np][3]),
+                          pack_half2(Sm[mt][2 * np + 1][0], Sm[mt][2 * np + 1][1]),
+                          pack_half2(Sm[mt][2 * np + 1][2], Sm[mt][2 * np + 1][3]));
+            }
+    };
+    // B fragments of S for U = w S^T: [ks][nt][b0, b1]
+    uint32_t Sf[8][NT][2];
+    auto load_sfrag = [&](int b) {
+        const uint32_t s16 = s16_slot(b);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int kk = 32 * wr + 16 * mt + g + 8 * (e >> 1);
-                    const int vv = 8 * nt + 2 * tq + (e & 1);
-                    const __half hv = __float2half_rn(Sm[mt][nt][e]);
-                    asm volatile("st.shared.b16 [%0], %1;" ::"r"(s16 + sw128_off(vv, kk, 16)),
-                                 "h"(*reinterpret_cast<const unsigned short*>(&hv)));
-                }
+        for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+            for (int np = 0; np < NT / 2; ++np)
+                ldsm_x4(s16 + sw128_off(16 * np + rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1), VS),
+                        Sf[ks][2 * np][0], Sf[ks][2 * np][1], Sf[ks][2 * np + 1][0],
+                        Sf[ks][2 * np + 1][1]);
     };
 
-    // B fragments of S for U = w S^T and qg S^T: [ks][4] = b0,b1 (nt 0), b0,b1 (nt 1)
-    uint32_t Sf[8][4];
-    auto load_sfrag = [&]() {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const int row = rr + 8 * (mi >> 1);
-            const int col = 16 * ks + 8 * (mi & 1);
-            ldsm_x4(s16 + sw128_off(row, col, 16), Sf[ks][0], Sf[ks][1], Sf[ks][2], Sf[ks][3]);
-        }
-    };
-
-    write_s16();
-    __syncthreads();  // consumers and producer: mbarriers initialised, S16 written
-    load_sfrag();
+    write_s16(0);
+    state_sync();
+    load_sfrag(0);
 
     bool failed = false;
     for (int lc = 0; lc < nch; ++lc) {
-        const int stage = lc & 1;
-        // Bounded wait; the outcome is voted at the next compute-warp barrier so
-        // that every compute warp leaves the walk together (nothing is written
-        // to global memory before that vote).
-        const bool ok = mbar_wait(&bars[stage], (lc >> 1) & 1);
-        const uint32_t st = sm_base + stage * L::kStage;
-        const uint32_t tw = st + kWsWOff, tqg = st + kWsQGOff, tkg = st + kWsKGOff;
-        const uint32_t taqk = st + kWsAqkOff;
-        const float* gam = reinterpret_cast<const float*>(smem + stage * L::kStage + kWsGammaOff);
-        const uint32_t tu = st + L::kSharedPad + gi * kWsUSliceBytes;  // [64][16] fp16
+        const int b = lc & 1;
+        const uint32_t par = (lc >> 1) & 1;
+        const bool ok = mbar_wait(&full[b], par);  // outcome voted below, before any write
+        const uint32_t st = stage_base(b);
+        const uint32_t tw = st + kWsWOff, tkg = st + kWsKGOff;
+        const float* gam = reinterpret_cast<const float*>(smem + b * L::kStage + kWsGammaOff);
+        const uint32_t tu = st + L::kSharedPad;  // [VS/16][64][16] fp16
+        const uint32_t ut = ut_slot(b);
 
-        // (1) accU = w S^T, accO = qg S^T for rows 16wr..16wr+15
-        // two independent accumulation chains per product (key halves) for ILP
-        float accU[2][4] = {}, accO[2][4] = {}, accU2[2][4] = {}, accO2[2][4] = {};
+        // U = u - w S^T for chunk rows 16wr..16wr+15 (two chains over the key halves)
+        float accU[NT][4] = {}, accU2[NT][4] = {};
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-            uint32_t aw[4], aq[4];
-            const int row = 16 * wr + rr + 8 * (mi & 1);
-            const int col = 16 * ks + 8 * (mi >> 1);
-            ldsm_x4(tw + sw128_off(row, col, 64), aw[0], aw[1], aw[2], aw[3]);
-            ldsm_x4(tqg + sw128_off(row, col, 64), aq[0], aq[1], aq[2], aq[3]);
-            float (*u)[4] = (ks & 1) ? accU2 : accU;
-            float (*o)[4] = (ks & 1) ? accO2 : accO;
-            mma_f16(u[0], aw, Sf[ks][0], Sf[ks][1]);
-            mma_f16(u[1], aw, Sf[ks][2], Sf[ks][3]);
-            mma_f16(o[0], aq, Sf[ks][0], Sf[ks][1]);
-            mma_f16(o[1], aq, Sf[ks][2], Sf[ks][3]);
+            uint32_t a[4];
+            ldsm_x4(tw + sw128_off(16 * wr + rr + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1), 64), a[0],
+                    a[1], a[2], a[3]);
+            float (*d)[4] = (ks & 1) ? accU2 : accU;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_f16(d[nt], a, Sf[ks][nt][0], Sf[ks][nt][1]);
         }
+        uint32_t uf[NT][2];  // U as fp16 pairs: [nt][rows g, g + 8]
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                accU[nt][e] += accU2[nt][e];
-                accO[nt][e] += accO2[nt][e];
-            }
-        // (2) U = u - accU, (3) U^T -> shared (fp16)
-        float U[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const int i = 16 * wr + g + 8 * hh;
                 const int vv = 8 * nt + 2 * tq;
                 uint32_t uv;
-                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(uv) : "r"(tu + i * 32 + vv * 2));
-                const float2 uf = __half22float2(*reinterpret_cast<__half2*>(&uv));
-                U[nt][2 * hh] = uf.x - accU[nt][2 * hh];
-                U[nt][2 * hh + 1] = uf.y - accU[nt][2 * hh + 1];
-                const __half h0 = __float2half_rn(U[nt][2 * hh]);
-                const __half h1 = __float2half_rn(U[nt][2 * hh + 1]);
-                asm volatile("st.shared.b16 [%0], %1;" ::"r"(ut + sw64_off(vv, i)),
-                             "h"(*reinterpret_cast<const unsigned short*>(&h0)));
-                asm volatile("st.shared.b16 [%0], %1;" ::"r"(ut + sw64_off(vv + 1, i)),
-                             "h"(*reinterpret_cast<const unsigned short*>(&h1)));
+                asm volatile("ld.shared.b32 %0, [%1];"
+                             : "=r"(uv)
+                             : "r"(tu + (vv >> 4) * kWsUSliceBytes + (i * 16 + (vv & 15)) * 2));
+                const float2 u2 = __half22float2(*reinterpret_cast<__half2*>(&uv));
+                uf[nt][hh] = pack_half2(u2.x - accU[nt][2 * hh] - accU2[nt][2 * hh],
+                                        u2.y - accU[nt][2 * hh + 1] - accU2[nt][2 * hh + 1]);
             }
-        if (consumer_sync_or(!ok)) {  // a copy never landed: report, stop the walk
+        // U^T into ring slot b (rows v, columns c): stmatrix transposes 8x8 blocks
+#pragma unroll
+        for (int np = 0; np < NT / 2; ++np) {
+            const int vrow = 16 * np + 8 * (mi >> 1) + rr;
+            const int ccol = 16 * wr + 8 * (mi & 1);
+            stsm_x4_t(ut + sw64_off(vrow, ccol), uf[2 * np][0], uf[2 * np][1], uf[2 * np + 1][0],
+                      uf[2 * np + 1][1]);
+        }
+        if (state_sync_or(!ok)) {  // a copy never landed: report, stop the walk
             failed = true;
             if (tid == 0 && p.status) atomicOr(p.status, 1);
             break;
         }
+        if (tid == 0) mbar_arrive(&sready[b]);  // S (published last step) and U of this chunk
 
-        // (5) o = accO + A_qk U (A_qk lower triangular: key blocks 0..wr)
+        // dS^T = kg^T U for key channels 32wr..32wr+31; S = gamma S + dS
+        float accS[2][NT][4] = {};
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-            if (ks > wr) break;
-            uint32_t a[4], b[4];
-            const int row = 16 * wr + rr + 8 * (mi & 1);
-            const int col = 16 * ks + 8 * (mi >> 1);
-            ldsm_x4(taqk + sw64_off(row, col), a[0], a[1], a[2], a[3]);
-            ldsm_x4(ut + sw64_off(rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1)), b[0], b[1], b[2],
-                    b[3]);
-            mma_f16(accO[0], a, b[0], b[1]);
-            mma_f16(accO[1], a, b[2], b[3]);
-        }
+            uint32_t bb[NT][2];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int i = 16 * wr + g + 8 * hh;
-            if (lc * C + i < len) {
-                const size_t t = (size_t)(tok0 + lc * C + i);
-                __nv_bfloat16* orow = p.out + (t * p.H + h) * D + vcol0;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const uint32_t pv = pack_bf162(accO[nt][2 * hh], accO[nt][2 * hh + 1]);
-                    *reinterpret_cast<uint32_t*>(orow + 8 * nt + 2 * tq) = pv;
-                }
-            }
-        }
-
-        // (6) dS^T = kg^T U for key channels 32wr..32wr+31, (7) S = gamma S + dS
-        float accS[2][2][4] = {};
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            uint32_t b[4];
-            ldsm_x4(ut + sw64_off(rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1)), b[0], b[1], b[2],
-                    b[3]);
+            for (int np = 0; np < NT / 2; ++np)
+                ldsm_x4(ut + sw64_off(16 * np + rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1)),
+                        bb[2 * np][0], bb[2 * np][1], bb[2 * np + 1][0], bb[2 * np + 1][1]);
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
                 uint32_t a[4];
-                const int srow = 16 * ks + rr + 8 * (mi >> 1);       // chunk row c
-                const int scol = 32 * wr + 16 * mt + 8 * (mi & 1);   // key channel
-                ldsm_x4_t(tkg + sw128_off(srow, scol, 64), a[0], a[1], a[2], a[3]);
-                mma_f16(accS[mt][0], a, b[0], b[1]);
-                mma_f16(accS[mt][1], a, b[2], b[3]);
+                ldsm_x4_t(tkg + sw128_off(16 * ks + rr + 8 * (mi >> 1),
+                                          32 * wr + 16 * mt + 8 * (mi & 1), 64),
+                          a[0], a[1], a[2], a[3]);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_f16(accS[mt][nt], a, bb[nt][0], bb[nt][1]);
             }
         }
 #pragma unroll
@@ -296,66 +346,71 @@ __global__ void __launch_bounds__(128 * NG + 32, 1) kda_scan_mma(FwdParams p) {
             for (int hh = 0; hh < 2; ++hh) {
                 const float gk = gam[32 * wr + 16 * mt + g + 8 * hh];
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
+                for (int nt = 0; nt < NT; ++nt) {
                     Sm[mt][nt][2 * hh] = gk * Sm[mt][nt][2 * hh] + accS[mt][nt][2 * hh];
                     Sm[mt][nt][2 * hh + 1] = gk * Sm[mt][nt][2 * hh + 1] + accS[mt][nt][2 * hh + 1];
                 }
             }
-        // stage data fully consumed by this warp: release it to the producer
         __syncwarp();
-        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&bars[2 + stage])) : "memory");
-        write_s16();
-        consumer_sync();
-        load_sfrag();
-    }
+        if (lane == 0) mbar_arrive(&empty[b]);  // w, kg, gamma and u of this stage are read
 
+        // publish the next chunk's incoming S in the other slot once the output
+        // warps are done with the chunk that used it
+        const int nb = b ^ 1;
+        bool ok2 = true;
+        if (lc >= 1) ok2 = mbar_wait(&sfree[nb], ((lc - 1) >> 1) & 1);
+        if (ok2) write_s16(nb);
+        if (state_sync_or(!ok2)) {
+            failed = true;
+            if (tid == 0 && p.status) atomicOr(p.status, 1);
+            break;
+        }
+        load_sfrag(nb);
+    }
     if (failed) return;
+
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int kk = 32 * wr + 16 * mt + g + 8 * (e >> 1);
-                const int vv = vcol0 + 8 * nt + 2 * tq + (e & 1);
+                const int vv = v0 + 8 * nt + 2 * tq + (e & 1);
                 store_state(p.st_out, p.st_dtype, out_base + (size_t)vv * D + kk, Sm[mt][nt][e]);
             }
 }
 
-template <int NG>
-cudaError_t launch_scan_ng(const FwdParams& p, cudaStream_t s) {
-    using L = ScanSmem<NG>;
+template <int NT>
+cudaError_t launch_scan_nt(const FwdParams& p, cudaStream_t s) {
+    using L = ScanSmem<NT>;
     static unsigned configured = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 32 && !(configured & (1u << dev))) {
-        e = cudaFuncSetAttribute(kda_scan_mma<NG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(kda_scan_mma<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  L::kTotal);
         if (e != cudaSuccess) return e;
         configured |= 1u << dev;
     }
-    dim3 grid((unsigned)p.N, (unsigned)p.H, (unsigned)(8 / NG));
-    kda_scan_mma<NG><<<grid, 128 * NG + 32, L::kTotal, s>>>(p);
+    dim3 grid((unsigned)p.N, (unsigned)p.H, (unsigned)(D / L::VS));
+    kda_scan_mma<NT><<<grid, kThreads, L::kTotal, s>>>(p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 int scan_groups(int N, int H, int num_sms) {
-    // Finest value split that still leaves whole sequences x heads to fill the
-    // GPU: fewer groups per CTA when there are few (sequence, head) pairs.
+    // 16 value rows per CTA while (sequence, head) pairs are few enough for the
+    // finer split to fill the GPU, 32 otherwise.
     const long pairs = (long)N * H;
     return pairs * 8 <= 2L * num_sms ? 1 : 2;
 }
 
-cudaError_t launch_scan(const FwdParams& p, int ng, cudaStream_t s) {
+cudaError_t launch_scan(const FwdParams& p, int groups, cudaStream_t s) {
     if (p.N <= 0) return cudaSuccess;
-    switch (ng) {
-        case 1: return launch_scan_ng<1>(p, s);
-        case 2: return launch_scan_ng<2>(p, s);
-        default: return launch_scan_ng<2>(p, s);
-    }
+    return groups <= 1 ? launch_scan_nt<2>(p, s) : launch_scan_nt<4>(p, s);
 }
 
 }  // namespace kda
