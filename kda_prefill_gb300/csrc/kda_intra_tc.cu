@@ -274,8 +274,9 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
             }
         }
         __syncthreads();
-        // q, k, g of this item are consumed: load the next item's now
-        if (tid == 0 && nxt < n_items) issue_inputs(nxt);
+        // q, k, g of this item are consumed: load the next item's now (from a
+        // warp with little work in the tile phase)
+        if (tid == kThreads - 32 && nxt < n_items) issue_inputs(nxt);
 
         // ---- A tiles: diagonal blocks (warps 0-7, tf32), off-diagonal pairs
         //      (warps 8-15, fp16), block decay factors (warps 12-15) -------------
@@ -358,8 +359,13 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
         }
         __syncthreads();  // the fp32 and fp16 operand tiles are consumed
 
-        // ---- A_qk / A_kk into place, and the qg / kg / X pass -----------------
-        {
+        // ---- one phase, by role:
+        //   warps 0-7   A_qk / A_kk into place; the k-left diagonal warps (odd)
+        //               then invert their 16x16 block T_II = (I + A_II)^{-1} in
+        //               registers, the q-left ones (even) form Y = b v in place;
+        //   warps 8-15  qg and kg (16-byte stores to the workspace) and
+        //               X = b k^ e^G (shared), 32 channels of one row per thread.
+        if (warp < 8) {
             auto put = [&](int sel, int tI, int tJ, const float (&acc)[2][4]) {
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
@@ -387,88 +393,112 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
                         }
                     }
             };
-            if (warp < 8) {
-                put(warp & 1, warp >> 1, warp >> 1, accD);
+            const int I = warp >> 1;
+            put(warp & 1, I, I, accD);
+            fence_proxy_async();  // A_qk staging, read by the bulk store below
+            if (warp & 1) {
+                __syncwarp();
+                if (lane < 16) {
+                    const int col = lane;
+                    const float* Ad = reinterpret_cast<const float*>(smem + kAkd) + I * 256;
+                    float t[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float acc = (i == col) ? 1.f : 0.f;
+#pragma unroll
+                        for (int j = 0; j < i; ++j) acc -= Ad[i * 16 + j] * t[j];
+                        t[i] = acc;  // zero above the diagonal since t[j] = 0 for j < col
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        *reinterpret_cast<__half*>(smem + kT16 + sw64_off(16 * I + i, 16 * I + col)) =
+                            __float2half_rn(t[i]);
+                }
             } else {
-                const int n_my = (warp < 12) ? 2 : 1;
-                for (int q2 = 0; q2 < n_my; ++q2) {
-                    const int itm = (warp - 8) + 8 * q2;
-                    int tI, tJ;
-                    pair_of(itm >> 1, tI, tJ);
-                    put(itm & 1, tI, tJ, accO[q2]);
+                const bool ok_v = mbar_wait(&bar[1], n_local & 1);
+                if (!ok_v && p.status) atomicOr(p.status, 1);
+                const int t4 = (warp >> 1) * 32 + lane;  // 0..127 over the four even warps
+                for (int e = t4; e < C * 64; e += 128) {  // pairs of elements
+                    const int r = e >> 6, c2 = (e & 63) * 2;
+                    uint8_t* vp = smem + kV + sw128_off(r, c2, 64);
+                    const float2 vv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vp));
+                    *reinterpret_cast<uint32_t*>(vp) = pack_half2(beta[r] * vv.x, beta[r] * vv.y);
                 }
             }
-            // qg, kg (16-byte stores to the workspace) and X = b k^ e^G (shared)
-            const int r = (lane & 7) + 8 * (warp & 7);
-            const int cg = (lane >> 3) + 4 * (warp >> 3);  // 16-channel group
-            const int c0 = 16 * cg;
+        } else {
+            const int n_my = (warp < 12) ? 2 : 1;
+            for (int q2 = 0; q2 < n_my; ++q2) {
+                const int itm = (warp - 8) + 8 * q2;
+                int tI, tJ;
+                pair_of(itm >> 1, tI, tJ);
+                // off-diagonal results into place (same rules as above)
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int i = 16 * tI + g8 + 8 * hh;
+                        const int j = 16 * tJ + 8 * nt + 2 * tq;
+                        const float x0 = accO[q2][nt][2 * hh], x1 = accO[q2][nt][2 * hh + 1];
+                        if ((itm & 1) == 0) {
+                            *reinterpret_cast<uint32_t*>(smem + kAqkStage + sw64_off(i, j)) =
+                                pack_half2(x0, x1);
+                        } else {
+                            const float bi = -beta[i];
+                            *reinterpret_cast<uint32_t*>(smem + kNAk + sw64_off(i, j)) =
+                                pack_half2(bi * x0, bi * x1);
+                        }
+                    }
+            }
+            fence_proxy_async();  // as above, before the global stores that follow
+            const int t2 = tid - 256;
+            const int r = (lane & 7) + 8 * (t2 >> 5);  // 8 consecutive lanes: 8 rows
+            const int cg = lane >> 3;                   // 32-channel group
             const int Br = r >> 4;
             const float bt = beta[r];
-            float lq[16], lk[16], ro[16];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                *reinterpret_cast<float4*>(lq + 4 * j) =
-                    *reinterpret_cast<const float4*>(smem + kLq32 + sw128f_off(r, c0 + 4 * j, 64));
-                *reinterpret_cast<float4*>(lk + 4 * j) =
-                    *reinterpret_cast<const float4*>(smem + kLk32 + sw128f_off(r, c0 + 4 * j, 64));
-            }
+            for (int pass = 0; pass < 2; ++pass) {
+                const int c0 = 32 * cg + 16 * pass;
+                float lq[16], lk[16], ro[16], f1[16], f2[16];
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
-                half8_to_f32(*reinterpret_cast<const uint4*>(smem + kRO + sw128_off(r, c0 + 8 * j, 64)),
-                             ro + 8 * j);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                uint32_t oq[4], ok[4], ox[4];
-#pragma unroll
-                for (int e2 = 0; e2 < 4; ++e2) {
-                    const int e = 8 * j + 2 * e2;
-                    const float f1a = F1[Br * 128 + c0 + e], f1b = F1[Br * 128 + c0 + e + 1];
-                    const float f2a = F2[Br * 128 + c0 + e], f2b = F2[Br * 128 + c0 + e + 1];
-                    oq[e2] = pack_half2(lq[e] * f1a, lq[e + 1] * f1b);
-                    ok[e2] = pack_half2(ro[e] * f2a, ro[e + 1] * f2b);
-                    ox[e2] = pack_half2(bt * lk[e] * f1a, bt * lk[e + 1] * f1b);
+                for (int j = 0; j < 4; ++j) {
+                    *reinterpret_cast<float4*>(lq + 4 * j) =
+                        *reinterpret_cast<const float4*>(smem + kLq32 + sw128f_off(r, c0 + 4 * j, 64));
+                    *reinterpret_cast<float4*>(lk + 4 * j) =
+                        *reinterpret_cast<const float4*>(smem + kLk32 + sw128f_off(r, c0 + 4 * j, 64));
+                    *reinterpret_cast<float4*>(f1 + 4 * j) =
+                        *reinterpret_cast<const float4*>(F1 + Br * 128 + c0 + 4 * j);
+                    *reinterpret_cast<float4*>(f2 + 4 * j) =
+                        *reinterpret_cast<const float4*>(F2 + Br * 128 + c0 + 4 * j);
                 }
-                const uint32_t o = sw128_off(r, c0 + 8 * j, 64);
-                *reinterpret_cast<uint4*>(blk + kWsQGOff + o) = make_uint4(oq[0], oq[1], oq[2], oq[3]);
-                *reinterpret_cast<uint4*>(blk + kWsKGOff + o) = make_uint4(ok[0], ok[1], ok[2], ok[3]);
-                *reinterpret_cast<uint4*>(smem + kLQ + o) = make_uint4(ox[0], ox[1], ox[2], ox[3]);
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    half8_to_f32(*reinterpret_cast<const uint4*>(smem + kRO + sw128_off(r, c0 + 8 * j, 64)),
+                                 ro + 8 * j);
+                uint32_t oq[8], okg[8], ox[8];
+#pragma unroll
+                for (int e2 = 0; e2 < 8; ++e2) {
+                    const int e = 2 * e2;
+                    oq[e2] = pack_half2(lq[e] * f1[e], lq[e + 1] * f1[e + 1]);
+                    okg[e2] = pack_half2(ro[e] * f2[e], ro[e + 1] * f2[e + 1]);
+                    ox[e2] = pack_half2(bt * lk[e] * f1[e], bt * lk[e + 1] * f1[e + 1]);
+                }
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const uint32_t o = sw128_off(r, c0 + 8 * j, 64);
+                    *reinterpret_cast<uint4*>(smem + kLQ + o) =
+                        make_uint4(ox[4 * j], ox[4 * j + 1], ox[4 * j + 2], ox[4 * j + 3]);
+                    *reinterpret_cast<uint4*>(blk + kWsQGOff + o) =
+                        make_uint4(oq[4 * j], oq[4 * j + 1], oq[4 * j + 2], oq[4 * j + 3]);
+                    *reinterpret_cast<uint4*>(blk + kWsKGOff + o) =
+                        make_uint4(okg[4 * j], okg[4 * j + 1], okg[4 * j + 2], okg[4 * j + 3]);
+                }
             }
         }
-        fence_proxy_async();
         __syncthreads();
         if (tid == 0) {
             bulk_s2g(blk + kWsAqkOff, smem + kAqkStage, 8192);
             bulk_commit();
         }
-
-        // ---- diagonal inverses T_II = (I + A_II)^{-1} (warps 0-1, in registers)
-        //      and Y = b v in place (other warps) -------------------------------
-        if (warp < 2) {
-            const int I = 2 * warp + (lane >> 4), col = lane & 15;
-            const float* Ad = reinterpret_cast<const float*>(smem + kAkd) + I * 256;
-            float t[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float acc = (i == col) ? 1.f : 0.f;
-#pragma unroll
-                for (int j = 0; j < i; ++j) acc -= Ad[i * 16 + j] * t[j];
-                t[i] = acc;  // zero above the diagonal since t[j] = 0 for j < col
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                *reinterpret_cast<__half*>(smem + kT16 + sw64_off(16 * I + i, 16 * I + col)) =
-                    __float2half_rn(t[i]);
-        } else {
-            const bool ok_v = mbar_wait(&bar[1], n_local & 1);
-            if (!ok_v && p.status) atomicOr(p.status, 1);
-            for (int e = tid - 64; e < C * 64; e += kThreads - 64) {  // pairs of elements
-                const int r = e >> 6, c2 = (e & 63) * 2;
-                uint8_t* vp = smem + kV + sw128_off(r, c2, 64);
-                const float2 vv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vp));
-                *reinterpret_cast<uint32_t*>(vp) = pack_half2(beta[r] * vv.x, beta[r] * vv.y);
-            }
-        }
-        __syncthreads();
 
         // ---- w = (I + A_kk)^{-1} X and u = (I + A_kk)^{-1} Y by blocked forward
         //      substitution: R_I = X_I - sum_{J<I} A_IJ W_J, W_I = T_II R_I.  Warp

@@ -18,8 +18,9 @@
 //   * 4 output warps compute o from the ring one step behind (warp wr: chunk
 //     rows 16wr..16wr+15) and store it;
 //   * 1 producer warp streams each chunk's intermediates (w, qg, kg, A_qk,
-//     gamma and the CTA's u columns) by TMA bulk copies into a double-buffered
-//     stage.
+//     gamma and the CTA's u columns) by TMA bulk copies into a three-stage
+//     ring, and asks L2 for the chunks further ahead (a bulk L2 prefetch, each
+//     of the CTAs of a (sequence, head) taking its share of the shared part).
 // Hand-offs use mbarriers (stage full/empty, ring ready/free); the state warps
 // synchronise among themselves on a named barrier.  Products are warp-level
 // tensor-core MMAs (m16n8k16, fp16 operands, fp32 accumulation); fp16 tiles
@@ -38,6 +39,9 @@ constexpr int D = kD;
 
 constexpr int round1k(int x) { return (x + 1023) / 1024 * 1024; }
 
+constexpr int kStages = 3;    // chunk intermediates in flight per CTA
+constexpr int kPrefetch = 6;  // chunks ahead of the stage loads asked of L2
+
 template <int NT>
 struct ScanSmem {
     static constexpr int VS = 8 * NT;                        // value rows per CTA
@@ -45,7 +49,7 @@ struct ScanSmem {
     static constexpr int kSharedPad = round1k(kShared);
     static constexpr int kU = (VS / 16) * kWsUSliceBytes;    // the CTA's u columns
     static constexpr int kStage = kSharedPad + round1k(kU);
-    static constexpr int kS16 = 2 * kStage;                  // 2 slots x [VS][128] fp16
+    static constexpr int kS16 = kStages * kStage;            // 2 slots x [VS][128] fp16
     static constexpr int kS16Slot = VS * 256;
     static constexpr int kUt = kS16 + 2 * kS16Slot;          // 2 slots x [VS][64] fp16
     static constexpr int kUtSlot = VS * 128;
@@ -77,10 +81,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_scan_mma(FwdParams p) {
     using L = ScanSmem<NT>;
     constexpr int VS = L::VS;
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);  // [2]
-    uint64_t* empty = full + 2;                                     // [2]
-    uint64_t* sready = full + 4;                                    // [2]
-    uint64_t* sfree = full + 6;                                     // [2]
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);  // [kStages]
+    uint64_t* empty = full + kStages;                               // [kStages]
+    uint64_t* sready = full + 2 * kStages;                          // [2]
+    uint64_t* sfree = sready + 2;                                   // [2]
 
     const int n = blockIdx.x;
     const int h = blockIdx.y;
@@ -101,10 +105,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_scan_mma(FwdParams p) {
     auto ut_slot = [&](int b) { return sm_base + L::kUt + b * L::kUtSlot; };
 
     if (tid == 0) {
-        mbar_init(&full[0], 1);
-        mbar_init(&full[1], 1);
-        mbar_init(&empty[0], kStateWarps + kOutWarps);
-        mbar_init(&empty[1], kStateWarps + kOutWarps);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kStateWarps + kOutWarps);
+        }
         mbar_init(&sready[0], 1);
         mbar_init(&sready[1], 1);
         mbar_init(&sfree[0], kOutWarps);
@@ -116,12 +120,31 @@ __global__ void __launch_bounds__(kThreads, 1) kda_scan_mma(FwdParams p) {
     // ======================= producer warp ==================================
     if (warp == kStateWarps + kOutWarps) {
         if (lane == 0) {
+            // this CTA's share of the shared part for the L2 prefetch (16-byte units)
+            constexpr int kGroups = D / VS;
+            constexpr int kUnits = kWsSharedBytes / 16;
+            const int z = blockIdx.z;
+            const uint32_t pf_off = 16u * (uint32_t)(kUnits * z / kGroups);
+            const uint32_t pf_len = 16u * (uint32_t)(kUnits * (z + 1) / kGroups) - pf_off;
+            auto prefetch = [&](int lc) {
+                const size_t ch = (size_t)(c0 + lc) * p.H + h;
+                const uint8_t* src = p.ws + ch * kWsBytes;
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src + pf_off),
+                             "r"(pf_len)
+                             : "memory");
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                                 src + kWsUOff + (v0 / 16) * kWsUSliceBytes),
+                             "r"((uint32_t)L::kU)
+                             : "memory");
+            };
+            for (int lc = 0; lc < kPrefetch && lc < nch; ++lc) prefetch(lc);
             for (int lc = 0; lc < nch; ++lc) {
-                const int stage = lc & 1;
-                if (lc >= 2 && !mbar_wait(&empty[stage], ((lc >> 1) - 1) & 1)) {
+                const int stage = lc % kStages;
+                if (lc >= kStages && !mbar_wait(&empty[stage], ((lc / kStages) - 1) & 1)) {
                     if (p.status) atomicOr(p.status, 1);
                     break;
                 }
+                if (lc + kPrefetch < nch) prefetch(lc + kPrefetch);
                 const size_t ch = (size_t)(c0 + lc) * p.H + h;
                 const uint8_t* src = p.ws + ch * kWsBytes;
                 uint8_t* dst = smem + stage * L::kStage;
@@ -138,13 +161,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_scan_mma(FwdParams p) {
     if (warp >= kStateWarps) {
         const int wr = warp - kStateWarps;  // chunk rows 16wr..16wr+15
         for (int lc = 0; lc < nch; ++lc) {
-            const int b = lc & 1;
+            const int b = lc & 1, sg = lc % kStages;
             const uint32_t par = (lc >> 1) & 1;
-            if (!mbar_wait(&full[b], par) || !mbar_wait(&sready[b], par)) {
+            if (!mbar_wait(&full[sg], (lc / kStages) & 1) || !mbar_wait(&sready[b], par)) {
                 if (p.status) atomicOr(p.status, 1);
                 break;
             }
-            const uint32_t st = stage_base(b);
+            const uint32_t st = stage_base(sg);
             const uint32_t tqg = st + kWsQGOff, taqk = st + kWsAqkOff;
             const uint32_t s16 = s16_slot(b), ut = ut_slot(b);
             // qg S^T (two accumulation chains over the key halves) + A_qk U
@@ -182,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_scan_mma(FwdParams p) {
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&sfree[b]);
-                mbar_arrive(&empty[b]);
+                mbar_arrive(&empty[sg]);
             }
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
@@ -271,12 +294,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_scan_mma(FwdParams p) {
 
     bool failed = false;
     for (int lc = 0; lc < nch; ++lc) {
-        const int b = lc & 1;
-        const uint32_t par = (lc >> 1) & 1;
-        const bool ok = mbar_wait(&full[b], par);  // outcome voted below, before any write
-        const uint32_t st = stage_base(b);
+        const int b = lc & 1, sg = lc % kStages;
+        const bool ok = mbar_wait(&full[sg], (lc / kStages) & 1);  // voted below, before any write
+        const uint32_t st = stage_base(sg);
         const uint32_t tw = st + kWsWOff, tkg = st + kWsKGOff;
-        const float* gam = reinterpret_cast<const float*>(smem + b * L::kStage + kWsGammaOff);
+        const float* gam = reinterpret_cast<const float*>(smem + sg * L::kStage + kWsGammaOff);
         const uint32_t tu = st + L::kSharedPad;  // [VS/16][64][16] fp16
         const uint32_t ut = ut_slot(b);
 
@@ -352,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_scan_mma(FwdParams p) {
                 }
             }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[b]);  // w, kg, gamma and u of this stage are read
+        if (lane == 0) mbar_arrive(&empty[sg]);  // w, kg, gamma and u of this stage are read
 
         // publish the next chunk's incoming S in the other slot once the output
         // warps are done with the chunk that used it
