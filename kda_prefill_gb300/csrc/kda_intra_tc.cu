@@ -61,8 +61,9 @@ constexpr int kRd32 = 147456;  // k^ / P fp32 [64][128]; later A_qk, -A_kk, A_kk
 constexpr int kLQ = 180224;    // q^ P fp16, rows 16..63 ([48][128]); later X -> w ([64][128])
 constexpr int kLK = 192512;    // k^ P fp16, rows 16..63 ([48][128])
 constexpr int kRO = 204800;    // k^ E_B/P fp16, rows 0..63 ([64][128])
-constexpr int kSc = 221184;    // rq[64] rk[64] beta[64] | EB, F1, F2 [4][128] (fp32)
-constexpr int kBar = kSc + 768 + 3 * 2048;
+constexpr int kSc = 221184;    // rq[64] rk[64] beta[64] | EB, F1, F2 [4][128] (fp32) | E_1, E_2
+constexpr int kMid = kSc + 768 + 3 * 2048;  // E_1, E_2 fp16 [2][128]
+constexpr int kBar = kMid + 512;
 constexpr int kSmemBytes = kBar + 64;
 // Reuse of the k^/P area after the tile MMAs:
 constexpr int kAqkStage = kRd32;          // A_qk fp16 [64][64] tile, to store (8 KB)
@@ -74,12 +75,6 @@ struct IntraMaps {
     CUtensorMap q, k, v, g;
 };
 
-__device__ __forceinline__ float bf(const uint8_t* base, int r, int c) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(base + sw128_off(r, c, 64)));
-}
-__device__ __forceinline__ float f32t(const uint8_t* base, int r, int c) {
-    return *reinterpret_cast<const float*>(base + sw128f_off(r, c, 64));
-}
 
 __device__ __forceinline__ float sumsq_bf16x8(const uint4 v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -132,6 +127,7 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
     float* EB = beta + 64;  // [4][128] decay total of each 16-row block
     float* F1 = EB + 512;   // [4][128] decay of the blocks before B (e^G at the block start)
     float* F2 = F1 + 512;   // [4][128] decay of the blocks after B
+    __half* MIDh = reinterpret_cast<__half*>(smem + kMid);     // [2][128] E_1, E_2 in fp16
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBar);  // [0] q,k,g  [1] v
 
     const int tid = threadIdx.x;
@@ -157,9 +153,9 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
     }
     __syncthreads();
 
-    // TMA issue (thread 0).
-    auto issue_inputs = [&](int it) {
-        const int t0 = p.chunk_tok[it / H], h = it % H;
+    // TMA issue (one thread).
+    auto issue_inputs = [&](int it, int t0) {
+        const int h = it % H;
         mbar_arrive_expect_tx(&bar[0], 65536);
         tma_load_3d(smem + kQ, &maps.q, &bar[0], 0, h, t0);
         tma_load_3d(smem + kQ + 8192, &maps.q, &bar[0], 64, h, t0);
@@ -169,37 +165,70 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
         for (int qt = 0; qt < 4; ++qt)
             tma_load_3d(smem + kG + qt * 8192, &maps.g, &bar[0], 32 * qt, h, t0);
     };
-    auto issue_v = [&](int it) {
-        const int t0 = p.chunk_tok[it / H], h = it % H;
+    auto issue_v = [&](int it, int t0) {
+        const int h = it % H;
         mbar_arrive_expect_tx(&bar[1], 16384);
         tma_load_3d(smem + kV, &maps.v, &bar[1], 0, h, t0);
         tma_load_3d(smem + kV + 8192, &maps.v, &bar[1], 64, h, t0);
     };
-    auto load_braw = [&](int it) -> float {
-        const int ch = it / H, hh = it % H;
-        const int t0 = p.chunk_tok[ch];
-        const int ln = min(C, p.cu[p.chunk_seq[ch] + 1] - t0);
-        return (tid < ln) ? p.beta_raw[(size_t)(t0 + tid) * H + hh] : 0.f;
+    // first token and valid length of an item's chunk
+    auto item_tok = [&](int it) { return p.chunk_tok[it / H]; };
+    auto item_len = [&](int it, int t0) { return min(C, p.cu[p.chunk_seq[it / H] + 1] - t0); };
+
+    // A tile results of one warp into place: sel 0 = A_qk (to the staging tile,
+    // j <= i), sel 1 = A_kk (diagonal block in fp32 with j < i, off-diagonal
+    // blocks negated in fp16).
+    auto put = [&](int sel, int tI, int tJ, const float (&acc)[2][4]) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int i = 16 * tI + g8 + 8 * hh;
+                const int j = 16 * tJ + 8 * nt + 2 * tq;
+                float x0 = acc[nt][2 * hh], x1 = acc[nt][2 * hh + 1];
+                if (sel == 0) {
+                    if (tI == tJ) {
+                        if (j > i) x0 = 0.f;
+                        if (j + 1 > i) x1 = 0.f;
+                    }
+                    *reinterpret_cast<uint32_t*>(smem + kAqkStage + sw64_off(i, j)) = pack_half2(x0, x1);
+                } else if (tI == tJ) {
+                    float* d = reinterpret_cast<float*>(smem + kAkd) + tI * 256;
+                    const float bi = beta[i];
+                    *reinterpret_cast<float2*>(d + (i & 15) * 16 + (j & 15)) =
+                        make_float2((j >= i) ? 0.f : bi * x0, (j + 1 >= i) ? 0.f : bi * x1);
+                } else {
+                    const float bi = -beta[i];
+                    *reinterpret_cast<uint32_t*>(smem + kNAk + sw64_off(i, j)) =
+                        pack_half2(bi * x0, bi * x1);
+                }
+            }
     };
 
     const int first = blockIdx.x;
-    if (tid == 0 && first < n_items) {
-        issue_inputs(first);
-        issue_v(first);
+    int tok_next = 0, len_next = 0;
+    float braw_next = 0.f;
+    if (first < n_items) {
+        tok_next = item_tok(first);
+        len_next = item_len(first, tok_next);
+        if (tid == 0) {
+            issue_inputs(first, tok_next);
+            issue_v(first, tok_next);
+        }
+        if (tid < len_next) braw_next = p.beta_raw[(size_t)(tok_next + tid) * H + first % H];
     }
-    float braw_next = (tid < C && first < n_items) ? load_braw(first) : 0.f;
 
     int n_local = 0;
     for (int it = first; it < n_items; it += gridDim.x, ++n_local) {
-        const int chunk = it / H;
-        const int tok0 = p.chunk_tok[chunk];
-        const int seq = p.chunk_seq[chunk];
-        const int len = min(C, p.cu[seq + 1] - tok0);
+        const int len = len_next;
+        const float braw = braw_next;
         uint8_t* blk = p.ws + (size_t)it * kWsBytes;
         const int nxt = it + gridDim.x;
-
-        const float braw = braw_next;
-        if (tid < C && nxt < n_items) braw_next = load_braw(nxt);
+        // the next item's chunk metadata, loaded while this one runs
+        if (nxt < n_items) {
+            tok_next = item_tok(nxt);
+            len_next = item_len(nxt, tok_next);
+        }
 
         const bool ok_in = mbar_wait(&bar[0], n_local & 1);
         if (__syncthreads_or(!ok_in)) {
@@ -229,6 +258,10 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
                 rk[r] = valid ? rsqrtf(sk + 1e-6f) : 0.f;
             }
             if (tid < C) beta[tid] = (tid < len) ? __fdividef(1.f, 1.f + __expf(-braw)) : 0.f;
+            // beta of the next item (len_next <= 64, so only the first 64 threads load)
+            braw_next = (nxt < n_items && tid < len_next)
+                            ? p.beta_raw[(size_t)(tok_next + tid) * H + nxt % H]
+                            : 0.f;
             // the previous item's bulk stores must have read the staging areas
             // (u in the q^P area, A_qk in the k^/P area, w in the LQ area) before
             // this item's decay pass rewrites them
@@ -236,166 +269,202 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
         }
         __syncthreads();
 
-        // ---- decay pass per (16-row block, channel) ---------------------------
-        //   forward: a = e^{lb sigmoid(g)}, P; q^ P and k^ P (fp32 for the diagonal
+        // ---- decay pass (warps 0-7: 16-row block B, channels c0 and c0 + 1)
+        //   forward: a = e^{lb sigmoid(g)}, P; q^ P and k^ P (tf32 for the diagonal
         //   tiles, fp16 for the off-diagonal left operands); backward: R = P_end/P
-        //   (suffix product), k^ / P = k^ R / P_end (fp32) and k^ R (fp16).
-        {
-            const int B = tid >> 7, c = tid & 127;
-            float P = 1.f;
-            float a[16], kh[16];
+        //   (suffix product), k^ / P = k^ R / P_end (tf32) and k^ R (fp16).
+        //   Warps 8-15 meanwhile form Y = b v in place (fp16).
+        if (warp < 8) {
+            const int B = warp >> 1;
+            const int c0 = 64 * (warp & 1) + 2 * lane;
+            float P0 = 1.f, P1 = 1.f;
+            float a0[16], a1[16], k0[16], k1[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int r = 16 * B + i;
-                const uint32_t o32 = sw128f_off(r, c, 64);
-                const float gr = *reinterpret_cast<const float*>(smem + kG + o32);
-                const float sg = __fdividef(1.f, 1.f + __expf(-gr));
-                a[i] = (r < len) ? __expf(lb * sg) : 1.f;
-                P *= a[i];
-                const float qh = bf(smem + kQ, r, c) * rq[r];
-                kh[i] = bf(smem + kK, r, c) * rk[r];
-                *reinterpret_cast<float*>(smem + kLq32 + o32) = qh * P;
-                *reinterpret_cast<float*>(smem + kLk32 + o32) = kh[i] * P;
+                const uint32_t o32 = sw128f_off(r, c0, 64);
+                const float2 gr = *reinterpret_cast<const float2*>(smem + kG + o32);
+                const bool valid = r < len;
+                const float s0 = __fdividef(1.f, 1.f + __expf(-gr.x));
+                const float s1 = __fdividef(1.f, 1.f + __expf(-gr.y));
+                a0[i] = valid ? __expf(lb * s0) : 1.f;
+                a1[i] = valid ? __expf(lb * s1) : 1.f;
+                P0 *= a0[i];
+                P1 *= a1[i];
+                const uint32_t o16 = sw128_off(r, c0, 64);
+                const uint32_t qw = *reinterpret_cast<const uint32_t*>(smem + kQ + o16);
+                const uint32_t kw = *reinterpret_cast<const uint32_t*>(smem + kK + o16);
+                const float sq = rq[r], sk = rk[r];
+                const float q0 = __uint_as_float(qw << 16) * sq * P0;
+                const float q1 = __uint_as_float(qw & 0xffff0000u) * sq * P1;
+                k0[i] = __uint_as_float(kw << 16) * sk;
+                k1[i] = __uint_as_float(kw & 0xffff0000u) * sk;
+                const float l0 = k0[i] * P0, l1 = k1[i] * P1;
+                *reinterpret_cast<uint2*>(smem + kLq32 + o32) = make_uint2(to_tf32(q0), to_tf32(q1));
+                *reinterpret_cast<uint2*>(smem + kLk32 + o32) = make_uint2(to_tf32(l0), to_tf32(l1));
                 if (B >= 1) {
-                    const uint32_t o16 = sw128_off(r - 16, c, 48);
-                    *reinterpret_cast<__half*>(smem + kLQ + o16) = __float2half_rn(qh * P);
-                    *reinterpret_cast<__half*>(smem + kLK + o16) = __float2half_rn(kh[i] * P);
+                    const uint32_t h16 = sw128_off(r - 16, c0, 48);
+                    *reinterpret_cast<uint32_t*>(smem + kLQ + h16) = pack_half2(q0, q1);
+                    *reinterpret_cast<uint32_t*>(smem + kLK + h16) = pack_half2(l0, l1);
                 }
             }
-            EB[B * 128 + c] = P;
-            const float inv_end = __fdividef(1.f, P);
-            float R = 1.f;
+            *reinterpret_cast<float2*>(EB + B * 128 + c0) = make_float2(P0, P1);
+            if (B == 1 || B == 2)
+                *reinterpret_cast<uint32_t*>(MIDh + (B - 1) * 128 + c0) = pack_half2(P0, P1);
+            const float ie0 = __fdividef(1.f, P0), ie1 = __fdividef(1.f, P1);
+            float R0 = 1.f, R1 = 1.f;
 #pragma unroll
             for (int i = 15; i >= 0; --i) {
                 const int r = 16 * B + i;
-                *reinterpret_cast<float*>(smem + kRd32 + sw128f_off(r, c, 64)) = kh[i] * R * inv_end;
-                *reinterpret_cast<__half*>(smem + kRO + sw128_off(r, c, 64)) = __float2half_rn(kh[i] * R);
-                R *= a[i];
+                const float x0 = k0[i] * R0, x1 = k1[i] * R1;
+                *reinterpret_cast<uint2*>(smem + kRd32 + sw128f_off(r, c0, 64)) =
+                    make_uint2(to_tf32(x0 * ie0), to_tf32(x1 * ie1));
+                *reinterpret_cast<uint32_t*>(smem + kRO + sw128_off(r, c0, 64)) = pack_half2(x0, x1);
+                R0 *= a0[i];
+                R1 *= a1[i];
+            }
+        } else {
+            const bool ok_v = mbar_wait(&bar[1], n_local & 1);
+            if (!ok_v && p.status) atomicOr(p.status, 1);
+            const int t2 = tid - 256;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {  // 16-byte pieces: 64 rows x 16
+                const int pc = t2 + 256 * e;
+                const int r = pc >> 4, c8 = (pc & 15) * 8;
+                uint4* vp = reinterpret_cast<uint4*>(smem + kV + sw128_off(r, c8, 64));
+                uint4 raw = *vp;
+                uint32_t* w4 = reinterpret_cast<uint32_t*>(&raw);
+                const float br = beta[r];
+#pragma unroll
+                for (int x = 0; x < 4; ++x)
+                    w4[x] = pack_half2(br * __uint_as_float(w4[x] << 16),
+                                       br * __uint_as_float(w4[x] & 0xffff0000u));
+                *vp = raw;
             }
         }
         __syncthreads();
-        // q, k, g of this item are consumed: load the next item's now (from a
-        // warp with little work in the tile phase)
-        if (tid == kThreads - 32 && nxt < n_items) issue_inputs(nxt);
+        // q, k, g of this item are consumed: load the next item's now
+        if (tid == kThreads - 32 && nxt < n_items) issue_inputs(nxt, tok_next);
 
-        // ---- A tiles: diagonal blocks (warps 0-7, tf32), off-diagonal pairs
-        //      (warps 8-15, fp16), block decay factors (warps 12-15) -------------
-        float accD[2][4] = {};     // diagonal: [nt][e]
-        float accO[2][2][4] = {};  // off-diagonal: up to two items
+        // ---- A tiles: diagonal blocks (warps 0-7, tf32: block warp/2, q-left
+        //      or k-left), off-diagonal block pairs (warps 8-13, fp16, q-left and
+        //      k-left sharing the right operand), and warps 14-15: block decay
+        //      factors, gamma, qg and kg ----------------------------------------
+        float acc[2][2][4] = {};
         if (warp < 8) {
             const int I = warp >> 1, which = warp & 1;  // which: 0 = q-left (A_qk), 1 = k-left
-            const uint8_t* L = smem + (which ? kLk32 : kLq32);
-            const int r0 = 16 * I + g8, r1 = r0 + 8;
-#pragma unroll 4
+            const uint32_t Lb = smem_u32(smem + (which ? kLk32 : kLq32));
+            const uint32_t Rb = smem_u32(smem + kRd32);
+#pragma unroll 8
             for (int ks = 0; ks < 16; ++ks) {
-                const int cl = 8 * ks + tq, ch = cl + 4;
-                uint32_t a4[4], b[2][2];
-                a4[0] = to_tf32(f32t(L, r0, cl));
-                a4[1] = to_tf32(f32t(L, r1, cl));
-                a4[2] = to_tf32(f32t(L, r0, ch));
-                a4[3] = to_tf32(f32t(L, r1, ch));
-                b[0][0] = to_tf32(f32t(smem + kRd32, r0, cl));
-                b[0][1] = to_tf32(f32t(smem + kRd32, r0, ch));
-                b[1][0] = to_tf32(f32t(smem + kRd32, r1, cl));
-                b[1][1] = to_tf32(f32t(smem + kRd32, r1, ch));
-                mma_tf32(accD[0], a4, b[0][0], b[0][1]);
-                mma_tf32(accD[1], a4, b[1][0], b[1][1]);
+                uint32_t a4[4], b4[4];
+                ldsm_x4(Lb + sw128f_off(16 * I + rr + 8 * (mi & 1), 8 * ks + 4 * (mi >> 1), 64), a4[0],
+                        a4[1], a4[2], a4[3]);
+                ldsm_x4(Rb + sw128f_off(16 * I + rr + 8 * (mi >> 1), 8 * ks + 4 * (mi & 1), 64), b4[0],
+                        b4[1], b4[2], b4[3]);
+                mma_tf32(acc[0][0], a4, b4[0], b4[1]);
+                mma_tf32(acc[0][1], a4, b4[2], b4[3]);
+            }
+        } else if (warp < 14) {
+            int tI, tJ;
+            pair_of(warp - 8, tI, tJ);
+            // decay of the blocks strictly between J and I (blocks 1 and/or 2)
+            const bool use1 = tJ < 1 && 1 < tI, use2 = tJ < 2 && 2 < tI;
+            const uint32_t lq = smem_u32(smem + kLQ), lk = smem_u32(smem + kLK);
+            const uint32_t rt = smem_u32(smem + kRO);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                uint32_t aq[4], ak[4], b4[4];
+                const uint32_t ao =
+                    sw128_off(16 * (tI - 1) + rr + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1), 48);
+                ldsm_x4(lq + ao, aq[0], aq[1], aq[2], aq[3]);
+                ldsm_x4(lk + ao, ak[0], ak[1], ak[2], ak[3]);
+                ldsm_x4(rt + sw128_off(16 * tJ + rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1), 64), b4[0],
+                        b4[1], b4[2], b4[3]);
+                if (use1 || use2) {
+                    const int cc = 16 * ks + 2 * tq;
+                    const __half2* m1 = reinterpret_cast<const __half2*>(MIDh);
+                    const __half2* m2 = reinterpret_cast<const __half2*>(MIDh + 128);
+                    __half2 mlo, mhi;
+                    if (use1 && use2) {
+                        mlo = __hmul2(m1[cc >> 1], m2[cc >> 1]);
+                        mhi = __hmul2(m1[(cc + 8) >> 1], m2[(cc + 8) >> 1]);
+                    } else {
+                        const __half2* m = use1 ? m1 : m2;
+                        mlo = m[cc >> 1];
+                        mhi = m[(cc + 8) >> 1];
+                    }
+                    __half2* hq = reinterpret_cast<__half2*>(aq);
+                    __half2* hk = reinterpret_cast<__half2*>(ak);
+                    hq[0] = __hmul2(hq[0], mlo);
+                    hq[1] = __hmul2(hq[1], mlo);
+                    hq[2] = __hmul2(hq[2], mhi);
+                    hq[3] = __hmul2(hq[3], mhi);
+                    hk[0] = __hmul2(hk[0], mlo);
+                    hk[1] = __hmul2(hk[1], mlo);
+                    hk[2] = __hmul2(hk[2], mhi);
+                    hk[3] = __hmul2(hk[3], mhi);
+                }
+                mma_f16(acc[0][0], aq, b4[0], b4[1]);
+                mma_f16(acc[0][1], aq, b4[2], b4[3]);
+                mma_f16(acc[1][0], ak, b4[0], b4[1]);
+                mma_f16(acc[1][1], ak, b4[2], b4[3]);
             }
         } else {
-            const uint32_t rt = smem_u32(smem + kRO);
-            const int n_my = (warp < 12) ? 2 : 1;
+            const int t3 = tid - (kThreads - 64);  // 0..63
+            // F1, F2 and gamma = e^{G_C}
 #pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                if (q2 >= n_my) break;
-                const int itm = (warp - 8) + 8 * q2;  // warps 8-11: items w-8, w; 12-15: w-8
-                const int which = itm & 1;
-                int tI, tJ;
-                pair_of(itm >> 1, tI, tJ);
-                const uint32_t lt = smem_u32(smem + (which ? kLK : kLQ));
+            for (int e0 = 0; e0 < 512; e0 += 64) {
+                const int e = e0 + t3;
+                const int Bq = e >> 7, cq = e & 127;
+                float pre = 1.f, suf = 1.f;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    uint32_t a4[4], b4[4];
-                    ldsm_x4(lt + sw128_off(16 * (tI - 1) + rr + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1), 48),
-                            a4[0], a4[1], a4[2], a4[3]);
-                    if (tI - tJ >= 2) {
-                        const int cc = 16 * ks + 2 * tq;
-                        float m0 = 1.f, m1 = 1.f, m8 = 1.f, m9 = 1.f;
-                        for (int Bm = tJ + 1; Bm < tI; ++Bm) {
-                            m0 *= EB[Bm * 128 + cc];
-                            m1 *= EB[Bm * 128 + cc + 1];
-                            m8 *= EB[Bm * 128 + cc + 8];
-                            m9 *= EB[Bm * 128 + cc + 9];
-                        }
-                        const __half2 mlo = __floats2half2_rn(m0, m1);
-                        const __half2 mhi = __floats2half2_rn(m8, m9);
-                        __half2* ah = reinterpret_cast<__half2*>(a4);
-                        ah[0] = __hmul2(ah[0], mlo);
-                        ah[1] = __hmul2(ah[1], mlo);
-                        ah[2] = __hmul2(ah[2], mhi);
-                        ah[3] = __hmul2(ah[3], mhi);
-                    }
-                    ldsm_x4(rt + sw128_off(16 * tJ + rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1), 64),
-                            b4[0], b4[1], b4[2], b4[3]);
-                    mma_f16(accO[q2][0], a4, b4[0], b4[1]);
-                    mma_f16(accO[q2][1], a4, b4[2], b4[3]);
+                for (int Bm = 0; Bm < 4; ++Bm) {
+                    const float x = EB[Bm * 128 + cq];
+                    if (Bm < Bq) pre *= x;
+                    if (Bm > Bq) suf *= x;
                 }
+                F1[e] = pre;
+                F2[e] = suf;
+                if (Bq == 0) reinterpret_cast<float*>(blk + kWsGammaOff)[cq] = EB[e] * suf;
             }
-            if (warp >= 12) {
-                // F1, F2 and gamma = e^{G_C}
-                for (int e = tid - 384; e < 512; e += 128) {
-                    const int Bq = e >> 7, cq = e & 127;
-                    float pre = 1.f, suf = 1.f;
+            asm volatile("bar.sync 1, 64;" ::: "memory");  // F1, F2 complete (warps 14-15)
+            // qg = q^ e^G = (q^ P) F1 and kg = k^ e^{G_C - G} = (k^ R) F2, row t3
+            const int r = t3, Br = r >> 4;
+#pragma unroll 2
+            for (int cgp = 0; cgp < 16; ++cgp) {
+                const int c0 = 8 * cgp;
+                float lq[8], ro[8];
+                *reinterpret_cast<float4*>(lq) =
+                    *reinterpret_cast<const float4*>(smem + kLq32 + sw128f_off(r, c0, 64));
+                *reinterpret_cast<float4*>(lq + 4) =
+                    *reinterpret_cast<const float4*>(smem + kLq32 + sw128f_off(r, c0 + 4, 64));
+                half8_to_f32(*reinterpret_cast<const uint4*>(smem + kRO + sw128_off(r, c0, 64)), ro);
+                const float4 fa = *reinterpret_cast<const float4*>(F1 + Br * 128 + c0);
+                const float4 fb = *reinterpret_cast<const float4*>(F1 + Br * 128 + c0 + 4);
+                const float4 ga = *reinterpret_cast<const float4*>(F2 + Br * 128 + c0);
+                const float4 gb = *reinterpret_cast<const float4*>(F2 + Br * 128 + c0 + 4);
+                const float f1[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+                const float f2[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+                uint32_t oq[4], okg[4];
 #pragma unroll
-                    for (int Bm = 0; Bm < 4; ++Bm) {
-                        const float x = EB[Bm * 128 + cq];
-                        if (Bm < Bq) pre *= x;
-                        if (Bm > Bq) suf *= x;
-                    }
-                    F1[e] = pre;
-                    F2[e] = suf;
-                    if (Bq == 0) reinterpret_cast<float*>(blk + kWsGammaOff)[cq] = EB[e] * suf;
+                for (int e2 = 0; e2 < 4; ++e2) {
+                    oq[e2] = pack_half2(lq[2 * e2] * f1[2 * e2], lq[2 * e2 + 1] * f1[2 * e2 + 1]);
+                    okg[e2] = pack_half2(ro[2 * e2] * f2[2 * e2], ro[2 * e2 + 1] * f2[2 * e2 + 1]);
                 }
+                const uint32_t o = sw128_off(r, c0, 64);
+                *reinterpret_cast<uint4*>(blk + kWsQGOff + o) = make_uint4(oq[0], oq[1], oq[2], oq[3]);
+                *reinterpret_cast<uint4*>(blk + kWsKGOff + o) = make_uint4(okg[0], okg[1], okg[2], okg[3]);
             }
         }
-        __syncthreads();  // the fp32 and fp16 operand tiles are consumed
+        __syncthreads();  // the operand tiles are consumed (k^ P stays for X)
 
-        // ---- one phase, by role:
-        //   warps 0-7   A_qk / A_kk into place; the k-left diagonal warps (odd)
-        //               then invert their 16x16 block T_II = (I + A_II)^{-1} in
-        //               registers, the q-left ones (even) form Y = b v in place;
-        //   warps 8-15  qg and kg (16-byte stores to the workspace) and
-        //               X = b k^ e^G (shared), 32 channels of one row per thread.
+        // ---- results into place; then the k-left diagonal warps invert their
+        //      16x16 block T_II = (I + A_II)^{-1} (registers, 16 lanes), and
+        //      warps 8-15 form X = b k^ e^G (fp16, in the LQ area) --------------
         if (warp < 8) {
-            auto put = [&](int sel, int tI, int tJ, const float (&acc)[2][4]) {
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int i = 16 * tI + g8 + 8 * hh;
-                        const int j = 16 * tJ + 8 * nt + 2 * tq;
-                        float x0 = acc[nt][2 * hh], x1 = acc[nt][2 * hh + 1];
-                        if (sel == 0) {  // A_qk, j <= i
-                            if (tI == tJ) {
-                                if (j > i) x0 = 0.f;
-                                if (j + 1 > i) x1 = 0.f;
-                            }
-                            *reinterpret_cast<uint32_t*>(smem + kAqkStage + sw64_off(i, j)) =
-                                pack_half2(x0, x1);
-                        } else if (tI == tJ) {  // A_kk diagonal block, fp32, j < i
-                            float* d = reinterpret_cast<float*>(smem + kAkd) + tI * 256;
-                            const float bi = beta[i];
-                            d[(i & 15) * 16 + (j & 15)] = (j >= i) ? 0.f : bi * x0;
-                            d[(i & 15) * 16 + (j & 15) + 1] = (j + 1 >= i) ? 0.f : bi * x1;
-                        } else {  // -A_kk off-diagonal block, fp16
-                            const float bi = -beta[i];
-                            *reinterpret_cast<uint32_t*>(smem + kNAk + sw64_off(i, j)) =
-                                pack_half2(bi * x0, bi * x1);
-                        }
-                    }
-            };
             const int I = warp >> 1;
-            put(warp & 1, I, I, accD);
-            fence_proxy_async();  // A_qk staging, read by the bulk store below
+            put(warp & 1, I, I, acc[0]);
             if (warp & 1) {
                 __syncwarp();
                 if (lane < 16) {
@@ -404,52 +473,30 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
                     float t[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        float acc = (i == col) ? 1.f : 0.f;
+                        float arow[16];
 #pragma unroll
-                        for (int j = 0; j < i; ++j) acc -= Ad[i * 16 + j] * t[j];
-                        t[i] = acc;  // zero above the diagonal since t[j] = 0 for j < col
+                        for (int j4 = 0; j4 < 4; ++j4)
+                            if (4 * j4 < i)
+                                *reinterpret_cast<float4*>(arow + 4 * j4) =
+                                    *reinterpret_cast<const float4*>(Ad + i * 16 + 4 * j4);
+                        float s = (i == col) ? 1.f : 0.f;
+#pragma unroll
+                        for (int j = 0; j < i; ++j) s -= arow[j] * t[j];
+                        t[i] = s;  // zero above the diagonal since t[j] = 0 for j < col
                     }
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         *reinterpret_cast<__half*>(smem + kT16 + sw64_off(16 * I + i, 16 * I + col)) =
                             __float2half_rn(t[i]);
                 }
-            } else {
-                const bool ok_v = mbar_wait(&bar[1], n_local & 1);
-                if (!ok_v && p.status) atomicOr(p.status, 1);
-                const int t4 = (warp >> 1) * 32 + lane;  // 0..127 over the four even warps
-                for (int e = t4; e < C * 64; e += 128) {  // pairs of elements
-                    const int r = e >> 6, c2 = (e & 63) * 2;
-                    uint8_t* vp = smem + kV + sw128_off(r, c2, 64);
-                    const float2 vv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vp));
-                    *reinterpret_cast<uint32_t*>(vp) = pack_half2(beta[r] * vv.x, beta[r] * vv.y);
-                }
             }
         } else {
-            const int n_my = (warp < 12) ? 2 : 1;
-            for (int q2 = 0; q2 < n_my; ++q2) {
-                const int itm = (warp - 8) + 8 * q2;
+            if (warp < 14) {
                 int tI, tJ;
-                pair_of(itm >> 1, tI, tJ);
-                // off-diagonal results into place (same rules as above)
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int i = 16 * tI + g8 + 8 * hh;
-                        const int j = 16 * tJ + 8 * nt + 2 * tq;
-                        const float x0 = accO[q2][nt][2 * hh], x1 = accO[q2][nt][2 * hh + 1];
-                        if ((itm & 1) == 0) {
-                            *reinterpret_cast<uint32_t*>(smem + kAqkStage + sw64_off(i, j)) =
-                                pack_half2(x0, x1);
-                        } else {
-                            const float bi = -beta[i];
-                            *reinterpret_cast<uint32_t*>(smem + kNAk + sw64_off(i, j)) =
-                                pack_half2(bi * x0, bi * x1);
-                        }
-                    }
+                pair_of(warp - 8, tI, tJ);
+                put(0, tI, tJ, acc[0]);
+                put(1, tI, tJ, acc[1]);
             }
-            fence_proxy_async();  // as above, before the global stores that follow
             const int t2 = tid - 256;
             const int r = (lane & 7) + 8 * (t2 >> 5);  // 8 consecutive lanes: 8 rows
             const int cg = lane >> 3;                   // 32-channel group
@@ -458,42 +505,25 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
 #pragma unroll
             for (int pass = 0; pass < 2; ++pass) {
                 const int c0 = 32 * cg + 16 * pass;
-                float lq[16], lk[16], ro[16], f1[16], f2[16];
+                float lk[16], f1[16];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    *reinterpret_cast<float4*>(lq + 4 * j) =
-                        *reinterpret_cast<const float4*>(smem + kLq32 + sw128f_off(r, c0 + 4 * j, 64));
                     *reinterpret_cast<float4*>(lk + 4 * j) =
                         *reinterpret_cast<const float4*>(smem + kLk32 + sw128f_off(r, c0 + 4 * j, 64));
                     *reinterpret_cast<float4*>(f1 + 4 * j) =
                         *reinterpret_cast<const float4*>(F1 + Br * 128 + c0 + 4 * j);
-                    *reinterpret_cast<float4*>(f2 + 4 * j) =
-                        *reinterpret_cast<const float4*>(F2 + Br * 128 + c0 + 4 * j);
                 }
+                uint32_t ox[8];
+#pragma unroll
+                for (int e2 = 0; e2 < 8; ++e2)
+                    ox[e2] = pack_half2(bt * lk[2 * e2] * f1[2 * e2], bt * lk[2 * e2 + 1] * f1[2 * e2 + 1]);
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
-                    half8_to_f32(*reinterpret_cast<const uint4*>(smem + kRO + sw128_off(r, c0 + 8 * j, 64)),
-                                 ro + 8 * j);
-                uint32_t oq[8], okg[8], ox[8];
-#pragma unroll
-                for (int e2 = 0; e2 < 8; ++e2) {
-                    const int e = 2 * e2;
-                    oq[e2] = pack_half2(lq[e] * f1[e], lq[e + 1] * f1[e + 1]);
-                    okg[e2] = pack_half2(ro[e] * f2[e], ro[e + 1] * f2[e + 1]);
-                    ox[e2] = pack_half2(bt * lk[e] * f1[e], bt * lk[e + 1] * f1[e + 1]);
-                }
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const uint32_t o = sw128_off(r, c0 + 8 * j, 64);
-                    *reinterpret_cast<uint4*>(smem + kLQ + o) =
+                    *reinterpret_cast<uint4*>(smem + kLQ + sw128_off(r, c0 + 8 * j, 64)) =
                         make_uint4(ox[4 * j], ox[4 * j + 1], ox[4 * j + 2], ox[4 * j + 3]);
-                    *reinterpret_cast<uint4*>(blk + kWsQGOff + o) =
-                        make_uint4(oq[4 * j], oq[4 * j + 1], oq[4 * j + 2], oq[4 * j + 3]);
-                    *reinterpret_cast<uint4*>(blk + kWsKGOff + o) =
-                        make_uint4(okg[4 * j], okg[4 * j + 1], okg[4 * j + 2], okg[4 * j + 3]);
-                }
             }
         }
+        fence_proxy_async();  // the A_qk staging tile is read by the bulk store
         __syncthreads();
         if (tid == 0) {
             bulk_s2g(blk + kWsAqkOff, smem + kAqkStage, 8192);
@@ -573,7 +603,7 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
             bulk_s2g(blk + kWsWOff, smem + kLQ, 16384);
             bulk_s2g(blk + kWsUOff, smem + kLq32, 16384);
             bulk_commit();
-            if (nxt < n_items) issue_v(nxt);  // v of this item is consumed
+            if (nxt < n_items) issue_v(nxt, tok_next);  // v of this item is consumed
         }
     }
     if (tid == 0) bulk_wait_all();  // stores complete before the CTA releases its smem
