@@ -61,8 +61,8 @@ constexpr int kRd32 = 147456;  // k^ / P fp32 [64][128]; later A_qk, -A_kk, A_kk
 constexpr int kLQ = 180224;    // q^ P fp16, rows 16..63 ([48][128]); later X -> w ([64][128])
 constexpr int kLK = 192512;    // k^ P fp16, rows 16..63 ([48][128])
 constexpr int kRO = 204800;    // k^ E_B/P fp16, rows 0..63 ([64][128])
-constexpr int kSc = 221184;    // rq[64] rk[64] beta[64] | EB, F1, F2 [4][128] (fp32) | E_1, E_2
-constexpr int kMid = kSc + 768 + 3 * 2048;  // E_1, E_2 fp16 [2][128]
+constexpr int kSc = 221184;    // rq[64] rk[64] beta[64] | F1 [4][128] | HT [4][2][128] (fp32) | E_1, E_2
+constexpr int kMid = kSc + 768 + 2048 + 4096;  // E_1, E_2 fp16 [2][128]
 constexpr int kBar = kMid + 512;
 constexpr int kSmemBytes = kBar + 64;
 // Reuse of the k^/P area after the tile MMAs:
@@ -85,16 +85,6 @@ __device__ __forceinline__ float sumsq_bf16x8(const uint4 v) {
         s = fmaf(lo, lo, fmaf(hi, hi, s));
     }
     return s;
-}
-
-__device__ __forceinline__ void half8_to_f32(const uint4 v, float* o) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-        o[2 * i] = f.x;
-        o[2 * i + 1] = f.y;
-    }
 }
 
 __device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
@@ -124,9 +114,8 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
     float* rq = reinterpret_cast<float*>(smem + kSc);
     float* rk = rq + 64;
     float* beta = rk + 64;
-    float* EB = beta + 64;  // [4][128] decay total of each 16-row block
-    float* F1 = EB + 512;   // [4][128] decay of the blocks before B (e^G at the block start)
-    float* F2 = F1 + 512;   // [4][128] decay of the blocks after B
+    float* F1 = beta + 64;  // [4][128] decay of the blocks before B (e^G at the block start)
+    float* HT = F1 + 512;   // [4][2][128] decay product of each 8-row half block
     __half* MIDh = reinterpret_cast<__half*>(smem + kMid);     // [2][128] E_1, E_2 in fp16
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBar);  // [0] q,k,g  [1] v
 
@@ -269,77 +258,127 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
         }
         __syncthreads();
 
-        // ---- decay pass (warps 0-7: 16-row block B, channels c0 and c0 + 1)
-        //   forward: a = e^{lb sigmoid(g)}, P; q^ P and k^ P (tf32 for the diagonal
-        //   tiles, fp16 for the off-diagonal left operands); backward: R = P_end/P
-        //   (suffix product), k^ / P = k^ R / P_end (tf32) and k^ R (fp16).
-        //   Warps 8-15 meanwhile form Y = b v in place (fp16).
-        if (warp < 8) {
-            const int B = warp >> 1;
+        // ---- decay pass, all warps: thread (block B, row half hf, channels c0,
+        //      c0 + 1) over 8 rows.  Part 1: a = e^{lb sigmoid(g)}, the half's
+        //      product, and q^, k^ kept in registers; the halves exchange their
+        //      products.  Part 2: forward P (q^ P and k^ P: tf32 for the diagonal
+        //      tiles, fp16 for the off-diagonal left operands, qg = q^ e^G to the
+        //      workspace), backward R = product of a after the row in the block
+        //      (k^ R / E_B in tf32, k^ R in fp16, kg = k^ e^{G_C - G} to the
+        //      workspace).  Each thread also forms two 16-byte pieces of b v.
+        {
+            const int B = warp >> 2, hf = (warp >> 1) & 1;
             const int c0 = 64 * (warp & 1) + 2 * lane;
-            float P0 = 1.f, P1 = 1.f;
-            float a0[16], a1[16], k0[16], k1[16];
+            const int rb = 16 * B + 8 * hf;
+            float a0[8], a1[8], q0[8], q1[8], k0[8], k1[8];
+            float L0 = 1.f, L1 = 1.f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int r = 16 * B + i;
-                const uint32_t o32 = sw128f_off(r, c0, 64);
-                const float2 gr = *reinterpret_cast<const float2*>(smem + kG + o32);
+            for (int i = 0; i < 8; ++i) {
+                const int r = rb + i;
+                const float2 gr = *reinterpret_cast<const float2*>(smem + kG + sw128f_off(r, c0, 64));
                 const bool valid = r < len;
                 const float s0 = __fdividef(1.f, 1.f + __expf(-gr.x));
                 const float s1 = __fdividef(1.f, 1.f + __expf(-gr.y));
                 a0[i] = valid ? __expf(lb * s0) : 1.f;
                 a1[i] = valid ? __expf(lb * s1) : 1.f;
-                P0 *= a0[i];
-                P1 *= a1[i];
+                L0 *= a0[i];
+                L1 *= a1[i];
                 const uint32_t o16 = sw128_off(r, c0, 64);
                 const uint32_t qw = *reinterpret_cast<const uint32_t*>(smem + kQ + o16);
                 const uint32_t kw = *reinterpret_cast<const uint32_t*>(smem + kK + o16);
                 const float sq = rq[r], sk = rk[r];
-                const float q0 = __uint_as_float(qw << 16) * sq * P0;
-                const float q1 = __uint_as_float(qw & 0xffff0000u) * sq * P1;
+                q0[i] = __uint_as_float(qw << 16) * sq;
+                q1[i] = __uint_as_float(qw & 0xffff0000u) * sq;
                 k0[i] = __uint_as_float(kw << 16) * sk;
                 k1[i] = __uint_as_float(kw & 0xffff0000u) * sk;
+            }
+            *reinterpret_cast<float2*>(HT + (2 * B + hf) * 128 + c0) = make_float2(L0, L1);
+            {
+                const bool ok_v = mbar_wait(&bar[1], n_local & 1);
+                if (!ok_v && p.status) atomicOr(p.status, 1);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {  // 16-byte pieces of v: 64 rows x 16
+                    const int pc = tid + kThreads * e;
+                    const int r = pc >> 4, c8 = (pc & 15) * 8;
+                    uint4* vp = reinterpret_cast<uint4*>(smem + kV + sw128_off(r, c8, 64));
+                    uint4 raw = *vp;
+                    uint32_t* w4 = reinterpret_cast<uint32_t*>(&raw);
+                    const float br = beta[r];
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+                        w4[x] = pack_half2(br * __uint_as_float(w4[x] << 16),
+                                           br * __uint_as_float(w4[x] & 0xffff0000u));
+                    *vp = raw;
+                }
+            }
+            __syncthreads();
+            // block totals E_m = (first half) x (second half); F1 = product over
+            // blocks before B, F2 = product over blocks after B
+            float E0[4], E1[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float2 t0 = *reinterpret_cast<const float2*>(HT + (2 * m) * 128 + c0);
+                const float2 t1 = *reinterpret_cast<const float2*>(HT + (2 * m + 1) * 128 + c0);
+                E0[m] = t0.x * t1.x;
+                E1[m] = t0.y * t1.y;
+            }
+            float f10 = 1.f, f11 = 1.f, f20 = 1.f, f21 = 1.f;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                if (m < B) {
+                    f10 *= E0[m];
+                    f11 *= E1[m];
+                }
+                if (m > B) {
+                    f20 *= E0[m];
+                    f21 *= E1[m];
+                }
+            }
+            const float2 own0 = *reinterpret_cast<const float2*>(HT + (2 * B) * 128 + c0);
+            const float2 own1 = *reinterpret_cast<const float2*>(HT + (2 * B + 1) * 128 + c0);
+            const float eb0 = own0.x * own1.x, eb1 = own0.y * own1.y;
+            if (hf == 0) {
+                *reinterpret_cast<float2*>(F1 + B * 128 + c0) = make_float2(f10, f11);
+                if (B == 1 || B == 2)
+                    *reinterpret_cast<uint32_t*>(MIDh + (B - 1) * 128 + c0) = pack_half2(eb0, eb1);
+                if (B == 0)
+                    *reinterpret_cast<float2*>(blk + kWsGammaOff + 4 * c0) =
+                        make_float2(eb0 * f20, eb1 * f21);
+            }
+            // forward: P_i = (first-half product, for the second half) x prefix
+            float P0 = hf ? own0.x : 1.f, P1 = hf ? own0.y : 1.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = rb + i;
+                P0 *= a0[i];
+                P1 *= a1[i];
+                const float x0 = q0[i] * P0, x1 = q1[i] * P1;
                 const float l0 = k0[i] * P0, l1 = k1[i] * P1;
-                *reinterpret_cast<uint2*>(smem + kLq32 + o32) = make_uint2(to_tf32(q0), to_tf32(q1));
+                const uint32_t o32 = sw128f_off(r, c0, 64);
+                *reinterpret_cast<uint2*>(smem + kLq32 + o32) = make_uint2(to_tf32(x0), to_tf32(x1));
                 *reinterpret_cast<uint2*>(smem + kLk32 + o32) = make_uint2(to_tf32(l0), to_tf32(l1));
                 if (B >= 1) {
                     const uint32_t h16 = sw128_off(r - 16, c0, 48);
-                    *reinterpret_cast<uint32_t*>(smem + kLQ + h16) = pack_half2(q0, q1);
+                    *reinterpret_cast<uint32_t*>(smem + kLQ + h16) = pack_half2(x0, x1);
                     *reinterpret_cast<uint32_t*>(smem + kLK + h16) = pack_half2(l0, l1);
                 }
+                *reinterpret_cast<uint32_t*>(blk + kWsQGOff + sw128_off(r, c0, 64)) =
+                    pack_half2(x0 * f10, x1 * f11);
             }
-            *reinterpret_cast<float2*>(EB + B * 128 + c0) = make_float2(P0, P1);
-            if (B == 1 || B == 2)
-                *reinterpret_cast<uint32_t*>(MIDh + (B - 1) * 128 + c0) = pack_half2(P0, P1);
-            const float ie0 = __fdividef(1.f, P0), ie1 = __fdividef(1.f, P1);
-            float R0 = 1.f, R1 = 1.f;
+            // backward: R_i = product of a after row i in the block
+            const float ie0 = __fdividef(1.f, eb0), ie1 = __fdividef(1.f, eb1);
+            float R0 = hf ? 1.f : own1.x, R1 = hf ? 1.f : own1.y;
 #pragma unroll
-            for (int i = 15; i >= 0; --i) {
-                const int r = 16 * B + i;
+            for (int i = 7; i >= 0; --i) {
+                const int r = rb + i;
                 const float x0 = k0[i] * R0, x1 = k1[i] * R1;
                 *reinterpret_cast<uint2*>(smem + kRd32 + sw128f_off(r, c0, 64)) =
                     make_uint2(to_tf32(x0 * ie0), to_tf32(x1 * ie1));
-                *reinterpret_cast<uint32_t*>(smem + kRO + sw128_off(r, c0, 64)) = pack_half2(x0, x1);
+                const uint32_t o16 = sw128_off(r, c0, 64);
+                *reinterpret_cast<uint32_t*>(smem + kRO + o16) = pack_half2(x0, x1);
+                *reinterpret_cast<uint32_t*>(blk + kWsKGOff + o16) = pack_half2(x0 * f20, x1 * f21);
                 R0 *= a0[i];
                 R1 *= a1[i];
-            }
-        } else {
-            const bool ok_v = mbar_wait(&bar[1], n_local & 1);
-            if (!ok_v && p.status) atomicOr(p.status, 1);
-            const int t2 = tid - 256;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {  // 16-byte pieces: 64 rows x 16
-                const int pc = t2 + 256 * e;
-                const int r = pc >> 4, c8 = (pc & 15) * 8;
-                uint4* vp = reinterpret_cast<uint4*>(smem + kV + sw128_off(r, c8, 64));
-                uint4 raw = *vp;
-                uint32_t* w4 = reinterpret_cast<uint32_t*>(&raw);
-                const float br = beta[r];
-#pragma unroll
-                for (int x = 0; x < 4; ++x)
-                    w4[x] = pack_half2(br * __uint_as_float(w4[x] << 16),
-                                       br * __uint_as_float(w4[x] & 0xffff0000u));
-                *vp = raw;
             }
         }
         __syncthreads();
@@ -347,9 +386,8 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
         if (tid == kThreads - 32 && nxt < n_items) issue_inputs(nxt, tok_next);
 
         // ---- A tiles: diagonal blocks (warps 0-7, tf32: block warp/2, q-left
-        //      or k-left), off-diagonal block pairs (warps 8-13, fp16, q-left and
-        //      k-left sharing the right operand), and warps 14-15: block decay
-        //      factors, gamma, qg and kg ----------------------------------------
+        //      or k-left) and off-diagonal block pairs (warps 8-13, fp16, q-left
+        //      and k-left sharing the right operand) --------------------------------
         float acc[2][2][4] = {};
         if (warp < 8) {
             const int I = warp >> 1, which = warp & 1;  // which: 0 = q-left (A_qk), 1 = k-left
@@ -409,52 +447,6 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
                 mma_f16(acc[0][1], aq, b4[2], b4[3]);
                 mma_f16(acc[1][0], ak, b4[0], b4[1]);
                 mma_f16(acc[1][1], ak, b4[2], b4[3]);
-            }
-        } else {
-            const int t3 = tid - (kThreads - 64);  // 0..63
-            // F1, F2 and gamma = e^{G_C}
-#pragma unroll
-            for (int e0 = 0; e0 < 512; e0 += 64) {
-                const int e = e0 + t3;
-                const int Bq = e >> 7, cq = e & 127;
-                float pre = 1.f, suf = 1.f;
-#pragma unroll
-                for (int Bm = 0; Bm < 4; ++Bm) {
-                    const float x = EB[Bm * 128 + cq];
-                    if (Bm < Bq) pre *= x;
-                    if (Bm > Bq) suf *= x;
-                }
-                F1[e] = pre;
-                F2[e] = suf;
-                if (Bq == 0) reinterpret_cast<float*>(blk + kWsGammaOff)[cq] = EB[e] * suf;
-            }
-            asm volatile("bar.sync 1, 64;" ::: "memory");  // F1, F2 complete (warps 14-15)
-            // qg = q^ e^G = (q^ P) F1 and kg = k^ e^{G_C - G} = (k^ R) F2, row t3
-            const int r = t3, Br = r >> 4;
-#pragma unroll 2
-            for (int cgp = 0; cgp < 16; ++cgp) {
-                const int c0 = 8 * cgp;
-                float lq[8], ro[8];
-                *reinterpret_cast<float4*>(lq) =
-                    *reinterpret_cast<const float4*>(smem + kLq32 + sw128f_off(r, c0, 64));
-                *reinterpret_cast<float4*>(lq + 4) =
-                    *reinterpret_cast<const float4*>(smem + kLq32 + sw128f_off(r, c0 + 4, 64));
-                half8_to_f32(*reinterpret_cast<const uint4*>(smem + kRO + sw128_off(r, c0, 64)), ro);
-                const float4 fa = *reinterpret_cast<const float4*>(F1 + Br * 128 + c0);
-                const float4 fb = *reinterpret_cast<const float4*>(F1 + Br * 128 + c0 + 4);
-                const float4 ga = *reinterpret_cast<const float4*>(F2 + Br * 128 + c0);
-                const float4 gb = *reinterpret_cast<const float4*>(F2 + Br * 128 + c0 + 4);
-                const float f1[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
-                const float f2[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-                uint32_t oq[4], okg[4];
-#pragma unroll
-                for (int e2 = 0; e2 < 4; ++e2) {
-                    oq[e2] = pack_half2(lq[2 * e2] * f1[2 * e2], lq[2 * e2 + 1] * f1[2 * e2 + 1]);
-                    okg[e2] = pack_half2(ro[2 * e2] * f2[2 * e2], ro[2 * e2 + 1] * f2[2 * e2 + 1]);
-                }
-                const uint32_t o = sw128_off(r, c0, 64);
-                *reinterpret_cast<uint4*>(blk + kWsQGOff + o) = make_uint4(oq[0], oq[1], oq[2], oq[3]);
-                *reinterpret_cast<uint4*>(blk + kWsKGOff + o) = make_uint4(okg[0], okg[1], okg[2], okg[3]);
             }
         }
         __syncthreads();  // the operand tiles are consumed (k^ P stays for X)
