@@ -87,6 +87,13 @@ __device__ __forceinline__ float sumsq_bf16x8(const uint4 v) {
     return s;
 }
 
+// Nearest tf32 value (ties away from zero) of x, as its fp32 bit pattern: add
+// half a tf32 unit in the last place to the magnitude bits and clear the 13 bits
+// below tf32 precision (a carry into the exponent is the correct rounding).
+__device__ __forceinline__ uint32_t tf32_bits(float x) {
+    return (__float_as_uint(x) + 0x1000u) & 0xffffe000u;
+}
+
 __device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
                  "r"(smem_u32(src)), "r"(bytes)
@@ -355,8 +362,8 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
                 const float x0 = q0[i] * P0, x1 = q1[i] * P1;
                 const float l0 = k0[i] * P0, l1 = k1[i] * P1;
                 const uint32_t o32 = sw128f_off(r, c0, 64);
-                *reinterpret_cast<uint2*>(smem + kLq32 + o32) = make_uint2(to_tf32(x0), to_tf32(x1));
-                *reinterpret_cast<uint2*>(smem + kLk32 + o32) = make_uint2(to_tf32(l0), to_tf32(l1));
+                *reinterpret_cast<uint2*>(smem + kLq32 + o32) = make_uint2(tf32_bits(x0), tf32_bits(x1));
+                *reinterpret_cast<uint2*>(smem + kLk32 + o32) = make_uint2(tf32_bits(l0), tf32_bits(l1));
                 if (B >= 1) {
                     const uint32_t h16 = sw128_off(r - 16, c0, 48);
                     *reinterpret_cast<uint32_t*>(smem + kLQ + h16) = pack_half2(x0, x1);
@@ -373,7 +380,7 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
                 const int r = rb + i;
                 const float x0 = k0[i] * R0, x1 = k1[i] * R1;
                 *reinterpret_cast<uint2*>(smem + kRd32 + sw128f_off(r, c0, 64)) =
-                    make_uint2(to_tf32(x0 * ie0), to_tf32(x1 * ie1));
+                    make_uint2(tf32_bits(x0 * ie0), tf32_bits(x1 * ie1));
                 const uint32_t o16 = sw128_off(r, c0, 64);
                 *reinterpret_cast<uint32_t*>(smem + kRO + o16) = pack_half2(x0, x1);
                 *reinterpret_cast<uint32_t*>(blk + kWsKGOff + o16) = pack_half2(x0 * f20, x1 * f21);
@@ -523,70 +530,64 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
         }
 
         // ---- w = (I + A_kk)^{-1} X and u = (I + A_kk)^{-1} Y by blocked forward
-        //      substitution: R_I = X_I - sum_{J<I} A_IJ W_J, W_I = T_II R_I.  Warp
-        //      w owns 16 of the 256 columns of [X | Y]; the blocks of W overwrite
-        //      X (or Y) in place.  No CTA barrier: each warp reads only its columns.
+        //      substitution, in transposed form so that every operand between
+        //      steps stays in registers: warp w owns 16 of the 256 columns of
+        //      [X | Y] and forms, for I = 0..3,
+        //        R_I^T = X_I^T - sum_{J<I} W_J^T A_IJ^T,   W_I^T = R_I^T T_II^T
+        //      with the columns as the MMA rows.  An m16n8k16 accumulator holding
+        //      (column, row pair) is exactly the A fragment of the next product,
+        //      so R_I^T and the W_J^T feed the MMAs directly; X_I^T enters as
+        //      X_I^T times the identity.  W goes out through stmatrix.trans into
+        //      the staging tiles (w over X in the LQ area, u in the q^P area).
         {
             const bool isu = warp >= 8;
             const int n0 = 16 * (warp & 7);
-            uint8_t* xt = isu ? smem + kV : smem + kLQ;
-            const uint32_t xb = smem_u32(xt);
+            const uint32_t xb = smem_u32(smem + (isu ? kV : kLQ));
             const uint32_t nak = smem_u32(smem + kNAk), t16 = smem_u32(smem + kT16);
-            uint8_t* ustage = smem + kLq32 + (warp & 7) * kWsUSliceBytes;  // [64][16] fp16
+            const uint32_t ub = smem_u32(smem + kLq32 + (warp & 7) * kWsUSliceBytes);  // [64][16]
+            // identity B fragments: b0 of n-tile 0 and b1 of n-tile 1 hold ones
+            // where row 2tq or 2tq + 1 equals column g
+            const uint32_t id = ((2 * tq == g8) ? 0x3c00u : 0u) | ((2 * tq + 1 == g8) ? 0x3c000000u : 0u);
+            uint32_t wf[4][4];  // W_J^T as fp16 A fragments
 #pragma unroll
             for (int I = 0; I < 4; ++I) {
-                float acc[2][4];
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const uint32_t xv = *reinterpret_cast<const uint32_t*>(
-                            xt + sw128_off(16 * I + g8 + 8 * hh, n0 + 8 * nt + 2 * tq, 64));
-                        const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&xv));
-                        acc[nt][2 * hh] = xf.x;
-                        acc[nt][2 * hh + 1] = xf.y;
-                    }
-                for (int J = 0; J < I; ++J) {
-                    uint32_t a[4], b[4];
-                    ldsm_x4(nak + sw64_off(16 * I + rr + 8 * (mi & 1), 16 * J + 8 * (mi >> 1)), a[0],
-                            a[1], a[2], a[3]);
-                    ldsm_x4_t(xb + sw128_off(16 * J + rr + 8 * (mi & 1), n0 + 8 * (mi >> 1), 64), b[0],
-                              b[1], b[2], b[3]);
-                    mma_f16(acc[0], a, b[0], b[1]);
-                    mma_f16(acc[1], a, b[2], b[3]);
+                float acc[2][4] = {};
+                {
+                    uint32_t xa[4];
+                    ldsm_x4_t(xb + sw128_off(16 * I + 8 * (mi >> 1) + rr, n0 + 8 * (mi & 1), 64), xa[0],
+                              xa[1], xa[2], xa[3]);
+                    mma_f16(acc[0], xa, id, 0u);
+                    mma_f16(acc[1], xa, 0u, id);
                 }
-                __syncwarp();
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh)
-                        *reinterpret_cast<uint32_t*>(
-                            xt + sw128_off(16 * I + g8 + 8 * hh, n0 + 8 * nt + 2 * tq, 64)) =
-                            pack_half2(acc[nt][2 * hh], acc[nt][2 * hh + 1]);
-                __syncwarp();
+                for (int J = 0; J < I; ++J) {
+                    uint32_t b4[4];
+                    ldsm_x4(nak + sw64_off(16 * I + 8 * (mi >> 1) + rr, 16 * J + 8 * (mi & 1)), b4[0], b4[1],
+                            b4[2], b4[3]);
+                    mma_f16(acc[0], wf[J], b4[0], b4[1]);
+                    mma_f16(acc[1], wf[J], b4[2], b4[3]);
+                }
+                const uint32_t ra[4] = {pack_half2(acc[0][0], acc[0][1]), pack_half2(acc[0][2], acc[0][3]),
+                                        pack_half2(acc[1][0], acc[1][1]), pack_half2(acc[1][2], acc[1][3])};
                 float wv[2][4] = {};
                 {
-                    uint32_t a[4], b[4];
-                    ldsm_x4(t16 + sw64_off(16 * I + rr + 8 * (mi & 1), 16 * I + 8 * (mi >> 1)), a[0],
-                            a[1], a[2], a[3]);
-                    ldsm_x4_t(xb + sw128_off(16 * I + rr + 8 * (mi & 1), n0 + 8 * (mi >> 1), 64), b[0],
-                              b[1], b[2], b[3]);
-                    mma_f16(wv[0], a, b[0], b[1]);
-                    mma_f16(wv[1], a, b[2], b[3]);
+                    uint32_t b4[4];
+                    ldsm_x4(t16 + sw64_off(16 * I + 8 * (mi >> 1) + rr, 16 * I + 8 * (mi & 1)), b4[0], b4[1],
+                            b4[2], b4[3]);
+                    mma_f16(wv[0], ra, b4[0], b4[1]);
+                    mma_f16(wv[1], ra, b4[2], b4[3]);
                 }
-                __syncwarp();
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int i = 16 * I + g8 + 8 * hh;
-                        const int col = n0 + 8 * nt + 2 * tq;
-                        const uint32_t v2 = pack_half2(wv[nt][2 * hh], wv[nt][2 * hh + 1]);
-                        *reinterpret_cast<uint32_t*>(xt + sw128_off(i, col, 64)) = v2;
-                        if (isu)
-                            *reinterpret_cast<uint32_t*>(ustage + (i * 16 + 8 * nt + 2 * tq) * 2) = v2;
-                    }
-                __syncwarp();
+                wf[I][0] = pack_half2(wv[0][0], wv[0][1]);
+                wf[I][1] = pack_half2(wv[0][2], wv[0][3]);
+                wf[I][2] = pack_half2(wv[1][0], wv[1][1]);
+                wf[I][3] = pack_half2(wv[1][2], wv[1][3]);
+                __syncwarp();  // X_I of these columns is read: W_I may overwrite it
+                const int row = 16 * I + 8 * (mi >> 1) + rr;
+                if (isu)
+                    stsm_x4_t(ub + row * 32 + 16 * (mi & 1), wf[I][0], wf[I][1], wf[I][2], wf[I][3]);
+                else
+                    stsm_x4_t(xb + sw128_off(row, n0 + 8 * (mi & 1), 64), wf[I][0], wf[I][1], wf[I][2],
+                              wf[I][3]);
             }
         }
         fence_proxy_async();
