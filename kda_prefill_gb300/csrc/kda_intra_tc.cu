@@ -254,10 +254,6 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
                 rk[r] = valid ? rsqrtf(sk + 1e-6f) : 0.f;
             }
             if (tid < C) beta[tid] = (tid < len) ? __fdividef(1.f, 1.f + __expf(-braw)) : 0.f;
-            // beta of the next item (len_next <= 64, so only the first 64 threads load)
-            braw_next = (nxt < n_items && tid < len_next)
-                            ? p.beta_raw[(size_t)(tok_next + tid) * H + nxt % H]
-                            : 0.f;
             // the previous item's bulk stores must have read the staging areas
             // (u in the q^P area, A_qk in the k^/P area, w in the LQ area) before
             // this item's decay pass rewrites them
@@ -457,6 +453,11 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
             }
         }
         __syncthreads();  // the operand tiles are consumed (k^ P stays for X)
+
+        // beta of the next item (its chunk metadata has landed by now; len_next <=
+        // 64, so only the first 64 threads load)
+        braw_next = (nxt < n_items && tid < len_next) ? p.beta_raw[(size_t)(tok_next + tid) * H + nxt % H]
+                                                      : 0.f;
 
         // ---- results into place; then the k-left diagonal warps invert their
         //      16x16 block T_II = (I + A_II)^{-1} (registers, 16 lanes), and
