@@ -61,8 +61,8 @@ constexpr int kRd32 = 147456;  // k^ / P fp32 [64][128]; later A_qk, -A_kk, A_kk
 constexpr int kLQ = 180224;    // q^ P fp16, rows 16..63 ([48][128]); later X -> w ([64][128])
 constexpr int kLK = 192512;    // k^ P fp16, rows 16..63 ([48][128])
 constexpr int kRO = 204800;    // k^ E_B/P fp16, rows 0..63 ([64][128])
-constexpr int kSc = 221184;    // rq[64] rk[64] beta[64] | F1 [4][128] | HT [4][2][128] (fp32) | E_1, E_2
-constexpr int kMid = kSc + 768 + 2048 + 4096;  // E_1, E_2 fp16 [2][128]
+constexpr int kSc = 221184;    // beta[64] | NS [16][16] | F1 [4][128] | HT [4][2][128] (fp32) | E_1, E_2
+constexpr int kMid = kSc + 256 + 1024 + 2048 + 4096;  // E_1, E_2 fp16 [2][128]
 constexpr int kBar = kMid + 512;
 constexpr int kSmemBytes = kBar + 64;
 // Reuse of the k^/P area after the tile MMAs:
@@ -75,17 +75,6 @@ struct IntraMaps {
     CUtensorMap q, k, v, g;
 };
 
-
-__device__ __forceinline__ float sumsq_bf16x8(const uint4 v) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float s = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
-        s = fmaf(lo, lo, fmaf(hi, hi, s));
-    }
-    return s;
-}
 
 // Nearest tf32 value (ties away from zero) of x, as its fp32 bit pattern: add
 // half a tf32 unit in the last place to the magnitude bits and clear the 13 bits
@@ -118,10 +107,9 @@ __device__ __forceinline__ void pair_of(int pi, int& I, int& J) {
 __global__ void __launch_bounds__(kThreads, 1)
 kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    float* rq = reinterpret_cast<float*>(smem + kSc);
-    float* rk = rq + 64;
-    float* beta = rk + 64;
-    float* F1 = beta + 64;  // [4][128] decay of the blocks before B (e^G at the block start)
+    float* beta = reinterpret_cast<float*>(smem + kSc);
+    float* NS = beta + 64;  // [16 warps][16] row sums of squares over each warp's 64 channels
+    float* F1 = NS + 256;   // [4][128] decay of the blocks before B (e^G at the block start)
     float* HT = F1 + 512;   // [4][2][128] decay product of each 8-row half block
     __half* MIDh = reinterpret_cast<__half*>(smem + kMid);     // [2][128] E_1, E_2 in fp16
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBar);  // [0] q,k,g  [1] v
@@ -232,43 +220,16 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
             break;
         }
 
-        // ---- row norms (4 rows per warp, 8 lanes per row) and beta ---------
-        {
-            const int r = 4 * warp + (lane & 3);
-            const int cg = lane >> 2;
-            float sq = 0.f, sk = 0.f;
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int c = 16 * cg + 8 * j;
-                sq += sumsq_bf16x8(*reinterpret_cast<const uint4*>(smem + kQ + sw128_off(r, c, 64)));
-                sk += sumsq_bf16x8(*reinterpret_cast<const uint4*>(smem + kK + sw128_off(r, c, 64)));
-            }
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                sq += __shfl_xor_sync(0xffffffffu, sq, o);
-                sk += __shfl_xor_sync(0xffffffffu, sk, o);
-            }
-            if (cg == 0) {
-                const bool valid = r < len;
-                rq[r] = valid ? rsqrtf(sq + 1e-6f) * 0.08838834764831845f : 0.f;  // 1/sqrt(128)
-                rk[r] = valid ? rsqrtf(sk + 1e-6f) : 0.f;
-            }
-            if (tid < C) beta[tid] = (tid < len) ? __fdividef(1.f, 1.f + __expf(-braw)) : 0.f;
-            // the previous item's bulk stores must have read the staging areas
-            // (u in the q^P area, A_qk in the k^/P area, w in the LQ area) before
-            // this item's decay pass rewrites them
-            if (tid == 0) bulk_wait_read_all();
-        }
-        __syncthreads();
-
         // ---- decay pass, all warps: thread (block B, row half hf, channels c0,
         //      c0 + 1) over 8 rows.  Part 1: a = e^{lb sigmoid(g)}, the half's
-        //      product, and q^, k^ kept in registers; the halves exchange their
-        //      products.  Part 2: forward P (q^ P and k^ P: tf32 for the diagonal
-        //      tiles, fp16 for the off-diagonal left operands, qg = q^ e^G to the
-        //      workspace), backward R = product of a after the row in the block
-        //      (k^ R / E_B in tf32, k^ R in fp16, kg = k^ e^{G_C - G} to the
-        //      workspace).  Each thread also forms two 16-byte pieces of b v.
+        //      product, q and k kept in registers, and the rows' sums of squares
+        //      over the warp's 64 channels; the halves exchange their products
+        //      and the two warps of a row their sums.  Part 2: row norms, b v (two
+        //      16-byte pieces per thread), forward P (q^ P and k^ P: tf32 for the
+        //      diagonal tiles, fp16 for the off-diagonal left operands, qg =
+        //      q^ e^G to the workspace), backward R = product of a after the row
+        //      in the block (k^ R / E_B in tf32, k^ R in fp16, kg = k^ e^{G_C - G}
+        //      to the workspace).
         {
             const int B = warp >> 2, hf = (warp >> 1) & 1;
             const int c0 = 64 * (warp & 1) + 2 * lane;
@@ -289,13 +250,58 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
                 const uint32_t o16 = sw128_off(r, c0, 64);
                 const uint32_t qw = *reinterpret_cast<const uint32_t*>(smem + kQ + o16);
                 const uint32_t kw = *reinterpret_cast<const uint32_t*>(smem + kK + o16);
-                const float sq = rq[r], sk = rk[r];
-                q0[i] = __uint_as_float(qw << 16) * sq;
-                q1[i] = __uint_as_float(qw & 0xffff0000u) * sq;
-                k0[i] = __uint_as_float(kw << 16) * sk;
-                k1[i] = __uint_as_float(kw & 0xffff0000u) * sk;
+                q0[i] = __uint_as_float(qw << 16);
+                q1[i] = __uint_as_float(qw & 0xffff0000u);
+                k0[i] = __uint_as_float(kw << 16);
+                k1[i] = __uint_as_float(kw & 0xffff0000u);
             }
             *reinterpret_cast<float2*>(HT + (2 * B + hf) * 128 + c0) = make_float2(L0, L1);
+            {
+                // sums of squares of the 8 rows (value 2i: q, 2i + 1: k) over the
+                // warp's 64 channels: a halving butterfly leaves value lane / 2 in
+                // lanes 2v and 2v + 1
+                float x[16];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    x[2 * i] = fmaf(q0[i], q0[i], q1[i] * q1[i]);
+                    x[2 * i + 1] = fmaf(k0[i], k0[i], k1[i] * k1[i]);
+                }
+#pragma unroll
+                for (int w = 8; w >= 1; w >>= 1) {  // lane bit 16, 8, 4, 2
+                    const bool up = (lane & (2 * w)) != 0;
+#pragma unroll
+                    for (int j = 0; j < w; ++j) {
+                        const float send = up ? x[j] : x[j + w];
+                        const float keep = up ? x[j + w] : x[j];
+                        x[j] = keep + __shfl_xor_sync(0xffffffffu, send, 2 * w);
+                    }
+                }
+                x[0] += __shfl_xor_sync(0xffffffffu, x[0], 1);
+                if ((lane & 1) == 0) NS[warp * 16 + (lane >> 1)] = x[0];
+            }
+            if (tid < C) beta[tid] = (tid < len) ? __fdividef(1.f, 1.f + __expf(-braw)) : 0.f;
+            // the previous item's bulk stores must have read the staging areas
+            // (u in the q^P area, A_qk in the k^/P area, w in the LQ area) before
+            // part 2 rewrites them
+            if (tid == 0) bulk_wait_read_all();
+            __syncthreads();
+            {
+                // row norms: lane 2v (v = 2i + s) forms the norm factor of value v
+                // (row i, s = 0: q with 1/sqrt(K), 1: k), then all lanes take theirs
+                const int v = lane >> 1;
+                const float ssum = NS[warp * 16 + v] + NS[(warp ^ 1) * 16 + v];
+                float nf = (rb + (v >> 1) < len) ? rsqrtf(ssum + 1e-6f) : 0.f;
+                if ((v & 1) == 0) nf *= 0.08838834764831845f;  // 1/sqrt(128)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float sq = __shfl_sync(0xffffffffu, nf, 4 * i);
+                    const float sk = __shfl_sync(0xffffffffu, nf, 4 * i + 2);
+                    q0[i] *= sq;
+                    q1[i] *= sq;
+                    k0[i] *= sk;
+                    k1[i] *= sk;
+                }
+            }
             {
                 const bool ok_v = mbar_wait(&bar[1], n_local & 1);
                 if (!ok_v && p.status) atomicOr(p.status, 1);
@@ -314,7 +320,6 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
                     *vp = raw;
                 }
             }
-            __syncthreads();
             // block totals E_m = (first half) x (second half); F1 = product over
             // blocks before B, F2 = product over blocks after B
             float E0[4], E1[4];
