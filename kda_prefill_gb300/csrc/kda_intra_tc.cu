@@ -241,8 +241,13 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
                 const int r = rb + i;
                 const float2 gr = *reinterpret_cast<const float2*>(smem + kG + sw128f_off(r, c0, 64));
                 const bool valid = r < len;
-                const float s0 = __fdividef(1.f, 1.f + __expf(-gr.x));
-                const float s1 = __fdividef(1.f, 1.f + __expf(-gr.y));
+                // sigmoid of both channels from one reciprocal: with d = 1 + e^{-g}
+                // (g clamped to [-40, 40], where sigmoid is 0 or 1 to fp32 precision,
+                // so d0 d1 stays finite), s0 = d1 / (d0 d1) and s1 = d0 / (d0 d1)
+                const float d0 = 1.f + __expf(-fminf(fmaxf(gr.x, -40.f), 40.f));
+                const float d1 = 1.f + __expf(-fminf(fmaxf(gr.y, -40.f), 40.f));
+                const float rd = __fdividef(1.f, d0 * d1);
+                const float s0 = d1 * rd, s1 = d0 * rd;
                 a0[i] = valid ? __expf(lb * s0) : 1.f;
                 a1[i] = valid ? __expf(lb * s1) : 1.f;
                 L0 *= a0[i];
