@@ -24,15 +24,21 @@
 // 1/P stay in fp32 range, and these blocks run as tf32 MMAs (m16n8k8) on fp32
 // operand tiles for the extra mantissa the near-diagonal entries need.
 //
+// The decay pass runs on all warps, a thread taking 8 rows (half a block) of two
+// channels; the halves exchange their products, and the rows' sums of squares
+// (for the norms) are reduced in-warp and exchanged at the same barrier.
+//
 // The solve is a blocked forward substitution on the right-hand sides:
 // W_I = T_II (X_I - sum_{J<I} A_IJ W_J) with the 16x16 inverses T_II computed in
-// registers; each warp owns 16 of the 256 columns of [X | Y].
+// registers; each warp owns 16 of the 256 columns of [X | Y] and works in
+// transposed form, so that every intermediate stays an MMA fragment.
 //
 // Data movement: inputs by TMA tiled loads (3-D tensor maps over [T][H][128],
 // 128-byte swizzle); the next item's q, k, g are loaded as soon as the decay
-// pass has consumed the current ones, v one item ahead.  qg and kg go out as
-// 16-byte stores, w, u and A_qk are staged in shared memory in their
-// workspace layout and written by TMA bulk stores.
+// pass has consumed the current ones, v one item ahead.  qg and kg go out from
+// the decay pass as fp16 pairs (a warp writes 128 contiguous bytes of a row);
+// w, u and A_qk are staged in shared memory in their workspace layout and
+// written by TMA bulk stores.
 
 #include <cuda.h>
 
