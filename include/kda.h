@@ -121,6 +121,11 @@ KDA_API size_t kda_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_
  * state is their initial state, zeros without one).  Unselected slots and the
  * stride padding are untouched.
  *
+ * Sequences of more than 8 tokens run through the chunked kernels (intra-chunk
+ * tiles, then the state scan); sequences of at most 8 tokens (decode steps,
+ * empty sequences) run token by token in a third kernel with the state in
+ * fp32 registers.  Both compute the same recurrence; only rounding differs.
+ *
  * ROCm/aiter PR #5754, "Technical Details": state_cache fp32 V-first
  * [slots, H, V, K] with a possibly padded stride(0); int32 state_indices; bool
  * has_initial_state (false starts from zero and does not read a dirty slot);
@@ -204,7 +209,8 @@ KDA_API int kda_cache_entries(void);
  * (a few microseconds of overhead, no synchronisation).  kda_kernel_times()
  * waits for the recorded events, adds each kernel's elapsed time over the calls
  * since the last read into ms[i] (i = launch order: 0 = intra-chunk kernel,
- * 1 = state scan), stores the number of calls in *calls, the number of kernels
+ * 1 = state scan, 2 = token-by-token kernel for short sequences), stores the
+ * number of calls in *calls, the number of kernels
  * in *count, and clears the record.  Mirrors the per-kernel split the pages
  * report (ROCm/aiter PR #4741, "Performance": per-kernel microseconds per
  * layer-call).  Returns KDA_OK, KDA_ERR_INVALID_ARG or KDA_ERR_CUDA.

@@ -12,7 +12,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libkda.so")
 
-SOURCES = ["kda_api.cu", "kda_kernels.cu", "kda_intra.cu", "kda_intra_tc.cu", "kda_scan.cu"]
+SOURCES = ["kda_api.cu", "kda_kernels.cu", "kda_intra.cu", "kda_intra_tc.cu", "kda_scan.cu",
+           "kda_decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 

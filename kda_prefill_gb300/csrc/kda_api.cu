@@ -45,6 +45,10 @@ constexpr int kChunk = kda::kC;
 constexpr int kD = kda::kD;
 
 inline int64_t chunks_of(int64_t len) { return (len + kChunk - 1) / kChunk; }
+// Chunks a sequence gets in the chunked kernels: none when it is short enough
+// for the token-by-token kernel.
+inline bool is_short(int64_t len) { return len <= kda::kShortMax; }
+inline int64_t routed_chunks(int64_t len) { return is_short(len) ? 0 : chunks_of(len); }
 
 int64_t max_chunks(int64_t T, int32_t N) { return (T + kChunk - 1) / kChunk + N; }
 
@@ -84,20 +88,29 @@ int check_host_bounds(const int32_t* cu, int32_t N, int64_t T) {
 // ---------------------------------------------------------------------------
 struct MetaLayout {
     int64_t n_chunks = 0;
+    int32_t n_long = 0, n_short = 0;
     size_t off_cu = 0, off_seq_off = 0, off_chunk_seq = 0, off_chunk_tok = 0;  // int32 units
+    size_t off_long = 0, off_short = 0;
     size_t words = 0;
 };
 
 inline size_t align4(size_t w) { return (w + 3) & ~size_t(3); }  // 16-byte blocks
 
-MetaLayout meta_layout(int32_t N, int64_t n_chunks) {
+// Chunk count and routing of the sequences from host bounds.
+MetaLayout meta_layout(const int32_t* cu, int32_t N) {
     MetaLayout L;
-    L.n_chunks = n_chunks;
+    for (int32_t n = 0; n < N; ++n) {
+        const int64_t len = (int64_t)cu[n + 1] - cu[n];
+        L.n_chunks += routed_chunks(len);
+        if (is_short(len)) ++L.n_short; else ++L.n_long;
+    }
     size_t o = 0;
     L.off_cu = o;        o = align4(o + (size_t)N + 1);
     L.off_seq_off = o;   o = align4(o + (size_t)N + 1);
-    L.off_chunk_seq = o; o = align4(o + (size_t)n_chunks);
-    L.off_chunk_tok = o; o = align4(o + (size_t)n_chunks);
+    L.off_chunk_seq = o; o = align4(o + (size_t)L.n_chunks);
+    L.off_chunk_tok = o; o = align4(o + (size_t)L.n_chunks);
+    L.off_long = o;      o = align4(o + (size_t)N);
+    L.off_short = o;     o = align4(o + (size_t)N);
     L.words = std::max<size_t>(o, 4);
     return L;
 }
@@ -108,11 +121,16 @@ void meta_fill(const int32_t* cu, int32_t N, const MetaLayout& L, int32_t* buf) 
     int32_t* off = buf + L.off_seq_off;
     int32_t* cseq = buf + L.off_chunk_seq;
     int32_t* ctok = buf + L.off_chunk_tok;
+    int32_t* lng = buf + L.off_long;
+    int32_t* sht = buf + L.off_short;
     int64_t j = 0;
+    int32_t nl = 0, ns = 0;
     for (int32_t n = 0; n < N; ++n) {
         mcu[n] = cu[n];
         off[n] = (int32_t)j;
-        const int64_t nc = chunks_of((int64_t)cu[n + 1] - cu[n]);
+        const int64_t len = (int64_t)cu[n + 1] - cu[n];
+        if (is_short(len)) sht[ns++] = n; else lng[nl++] = n;
+        const int64_t nc = routed_chunks(len);
         for (int64_t c = 0; c < nc; ++c, ++j) {
             cseq[j] = n;
             ctok[j] = (int32_t)(cu[n] + c * kChunk);
@@ -240,12 +258,10 @@ class MetaCache {
         int rc = evict_if_full(stream);
         if (rc != KDA_OK) return rc;
 
-        int64_t n_chunks = 0;
-        for (int32_t n = 0; n < N; ++n) n_chunks += chunks_of((int64_t)cu[n + 1] - cu[n]);
         auto* m = new MetaEntry();
         m->key = std::move(key);
         m->device = dev;
-        m->layout = meta_layout(N, n_chunks);
+        m->layout = meta_layout(cu, N);
         const size_t bytes = m->layout.words * sizeof(int32_t);
         cudaEvent_t* done = nullptr;
         bool separate = false;
@@ -363,6 +379,7 @@ MetaCache& cache() {
 struct Timing {
     bool enabled = false;
     std::vector<std::vector<cudaEvent_t>> calls;  // kNumKernels + 1 marks per call
+    std::vector<unsigned> launched;               // per call: kernels that had work
     std::vector<cudaEvent_t> free_events;
 
     cudaEvent_t take() {
@@ -447,6 +464,10 @@ int run_forward(const void* q, const void* k, const void* v, const float* g_raw,
     p.seq_off = m->dev + m->layout.off_seq_off;
     p.chunk_seq = m->dev + m->layout.off_chunk_seq;
     p.chunk_tok = m->dev + m->layout.off_chunk_tok;
+    p.long_list = m->dev + m->layout.off_long;
+    p.short_list = m->dev + m->layout.off_short;
+    p.n_long = m->layout.n_long;
+    p.n_short = m->layout.n_short;
     p.ws = ws ? ws + kda::kWsHeader : nullptr;
     p.status = ws ? reinterpret_cast<int*>(ws) : nullptr;
     p.st_in = st.in;
@@ -470,7 +491,10 @@ int run_forward(const void* q, const void* k, const void* v, const float* g_raw,
         marks = ev.data();
     }
     e = kda::launch_forward(p, stream, marks);
-    if (marks) timing().calls.push_back(ev);
+    if (marks) {
+        timing().calls.push_back(ev);
+        timing().launched.push_back(kda::launched_kernels(p));
+    }
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     cache().mark_use(m, stream, capturing);
     return KDA_OK;
@@ -672,10 +696,13 @@ int kda_kernel_times(float* ms, int capacity, int* count, int* calls) {
     for (int i = 0; i < kda::kNumKernels; ++i) ms[i] = 0.f;
     Timing& t = timing();
     int rc = KDA_OK;
-    for (auto& c : t.calls) {
+    for (size_t j = 0; j < t.calls.size(); ++j) {
+        const auto& c = t.calls[j];
+        const unsigned ran = t.launched[j];
         cudaError_t e = cudaEventSynchronize(c.back());
         if (e != cudaSuccess) rc = cuda_fail(e, "cudaEventSynchronize");
         for (int i = 0; i < kda::kNumKernels && rc == KDA_OK; ++i) {
+            if (!(ran & (1u << i))) continue;  // not launched: no time
             float x = 0.f;
             e = cudaEventElapsedTime(&x, c[i], c[i + 1]);
             if (e != cudaSuccess) rc = cuda_fail(e, "cudaEventElapsedTime");
@@ -686,6 +713,7 @@ int kda_kernel_times(float* ms, int capacity, int* count, int* calls) {
     *calls = (int)t.calls.size();
     *count = kda::kNumKernels;
     t.calls.clear();
+    t.launched.clear();
     return rc;
 }
 
@@ -725,30 +753,43 @@ int noalloc_scratch(void** out) {
     return KDA_OK;
 }
 
-// Chunk table from the device bounds, one CTA: chunk counts, an exclusive
-// prefix sum in tiles of 1024 sequences, then each sequence's chunks.  Same
-// numbering as the host planner (chunks follow the sequence's position in
-// cu_seqlens; empty sequences own no chunk).
+// Chunk table and sequence routing from the device bounds, one CTA: per
+// sequence its chunk count and whether it is long (short sequences, at most
+// kShortMax tokens, get no chunk and go to the token-by-token kernel), two
+// inclusive prefix sums in tiles of 1024 sequences, then each sequence's
+// chunks and its place in the long or the short list.  Same numbering as the
+// host planner (chunks follow the sequence's position in cu_seqlens).
 __global__ void __launch_bounds__(1024) kda_noalloc_meta(const int32_t* cu, int N, int C,
                                                          int32_t* mcu, int32_t* off,
-                                                         int32_t* cseq, int32_t* ctok) {
+                                                         int32_t* cseq, int32_t* ctok,
+                                                         int32_t* lng, int32_t* sht) {
     __shared__ int32_t sbuf[1024];
-    __shared__ int32_t carry;
+    __shared__ int32_t lbuf[1024];
+    __shared__ int32_t carry, lcarry;
     const int tid = threadIdx.x;
-    if (tid == 0) carry = 0;
+    if (tid == 0) {
+        carry = 0;
+        lcarry = 0;
+    }
     __syncthreads();
     for (int base = 0; base < N; base += 1024) {
         const int n = base + tid;
-        const int nc = (n < N) ? (cu[n + 1] - cu[n] + C - 1) / C : 0;
+        const int len = (n < N) ? cu[n + 1] - cu[n] : 0;
+        const int is_long = (n < N && len > kda::kShortMax) ? 1 : 0;
+        const int nc = is_long ? (len + C - 1) / C : 0;
         sbuf[tid] = nc;
+        lbuf[tid] = is_long;
         __syncthreads();
         for (int o = 1; o < 1024; o <<= 1) {
             const int x = (tid >= o) ? sbuf[tid - o] : 0;
+            const int y = (tid >= o) ? lbuf[tid - o] : 0;
             __syncthreads();
             sbuf[tid] += x;
+            lbuf[tid] += y;
             __syncthreads();
         }
         const int excl = carry + sbuf[tid] - nc;
+        const int lpos = lcarry + lbuf[tid] - is_long;  // long sequences before n
         if (n < N) {
             mcu[n] = cu[n];
             off[n] = excl;
@@ -756,9 +797,16 @@ __global__ void __launch_bounds__(1024) kda_noalloc_meta(const int32_t* cu, int 
                 cseq[excl + c] = n;
                 ctok[excl + c] = cu[n] + c * C;
             }
+            if (is_long)
+                lng[lpos] = n;
+            else
+                sht[n - lpos] = n;
         }
         __syncthreads();
-        if (tid == 1023) carry += sbuf[1023];
+        if (tid == 1023) {
+            carry += sbuf[1023];
+            lcarry += lbuf[1023];
+        }
         __syncthreads();
     }
     if (tid == 0) {
@@ -783,11 +831,12 @@ extern "C" int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v
                     "kda_chunk_fwd_noalloc needs both cu_seqlens and cu_seqlens_host");
     if (num_seqs < 0 || total_tokens < 0 || num_heads <= 0)
         return fail(KDA_ERR_INVALID_ARG, "invalid sizes");
-    // scratch layout: [workspace][cu | seq_off | chunk_seq | chunk_tok]
+    // scratch layout: [workspace][cu | seq_off | chunk_seq | chunk_tok | long | short]
     const int64_t bound = max_chunks(total_tokens, num_seqs);
     const size_t ws_need = kda_workspace_size(total_tokens, num_seqs, num_heads);
     const size_t ws_part = (ws_need + 255) & ~size_t(255);
-    const size_t meta_words = 4 * (align4((size_t)num_seqs + 1) + align4((size_t)bound));
+    const size_t meta_words = 2 * align4((size_t)num_seqs + 1) + 2 * align4((size_t)bound) +
+                              2 * align4((size_t)num_seqs);
     const size_t need = ws_part + meta_words * sizeof(int32_t);
     if (need > (size_t)KDA_NOALLOC_SCRATCH_BYTES)
         return fail(KDA_ERR_WORKSPACE,
@@ -819,8 +868,12 @@ extern "C" int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v
                         "state_cache and its slot stride must be 16-byte aligned");
     }
     int64_t n_chunks = 0;
-    for (int32_t n = 0; n < num_seqs; ++n)
-        n_chunks += chunks_of((int64_t)cu_seqlens_host[n + 1] - cu_seqlens_host[n]);
+    int32_t n_long = 0;
+    for (int32_t n = 0; n < num_seqs; ++n) {
+        const int64_t len = (int64_t)cu_seqlens_host[n + 1] - cu_seqlens_host[n];
+        n_chunks += routed_chunks(len);
+        n_long += is_short(len) ? 0 : 1;
+    }
 
     uint8_t* base = static_cast<uint8_t*>(scratch);
     int32_t* meta = reinterpret_cast<int32_t*>(base + ws_part);
@@ -828,12 +881,14 @@ extern "C" int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v
     int32_t* off = mcu + align4((size_t)num_seqs + 1);
     int32_t* cseq = off + align4((size_t)num_seqs + 1);
     int32_t* ctok = cseq + align4((size_t)bound);
+    int32_t* lng = ctok + align4((size_t)bound);
+    int32_t* sht = lng + align4((size_t)num_seqs);
 
     cudaError_t e = cudaMemsetAsync(base, 0, sizeof(int), stream);  // status word
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (status)");
     if (num_seqs > 0) {
         kda_noalloc_meta<<<1, 1024, 0, stream>>>(cu_seqlens, num_seqs, kChunk, mcu, off, cseq,
-                                                  ctok);
+                                                  ctok, lng, sht);
         e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "chunk table kernel launch");
     }
@@ -853,6 +908,10 @@ extern "C" int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v
     p.seq_off = off;
     p.chunk_seq = cseq;
     p.chunk_tok = ctok;
+    p.long_list = lng;
+    p.short_list = sht;
+    p.n_long = n_long;
+    p.n_short = num_seqs - n_long;
     p.ws = base + kda::kWsHeader;
     p.status = reinterpret_cast<int*>(base);
     p.st_in = state_cache;

@@ -12,6 +12,9 @@ namespace kda {
 
 constexpr int kD = 128;  // K = V = head dimension
 constexpr int kC = 64;   // tokens per chunk
+// Sequences of at most kShortMax tokens (empty ones included) bypass the
+// chunked kernels and run token by token in kda_decode.
+constexpr int kShortMax = 8;
 
 // Workspace: one block of kWsBytes per (chunk, head), chunk-major
 // (block index = chunk * H + head).  Inside a block:
@@ -54,6 +57,13 @@ struct FwdParams {
     const int32_t* seq_off;    // [N+1] first chunk of each sequence
     const int32_t* chunk_seq;  // [n_chunks] sequence of each chunk
     const int32_t* chunk_tok;  // [n_chunks] first token of each chunk
+    // sequence routing: long_list (n_long) names the sequences the chunked
+    // kernels process, short_list (n_short) those kda_decode processes.  With
+    // long_list == nullptr every sequence goes through the chunked kernels.
+    const int32_t* long_list;
+    const int32_t* short_list;
+    int n_long;
+    int n_short;
 
     uint8_t* ws;   // chunk blocks (kWsBytes each)
     int* status;   // workspace header
@@ -75,17 +85,21 @@ inline size_t workspace_bytes(int64_t max_chunks, int H) {
 }
 
 // Number of kernels one forward launches, and their names (launch order).
-constexpr int kNumKernels = 2;
+constexpr int kNumKernels = 3;
 const char* kernel_name(int i);
 
 // Enqueues the kernels of one forward on `s`.  When `marks` is non-null it
 // holds kNumKernels + 1 events: marks[0] is recorded before the first kernel
 // and marks[i + 1] after kernel i.
 cudaError_t launch_forward(const FwdParams& p, cudaStream_t s, cudaEvent_t* marks);
+// Bit i set when kernel i (launch order) has work for these parameters; a
+// kernel without work is not launched and its timing interval is empty.
+unsigned launched_kernels(const FwdParams& p);
 
-// Individual stages (kda_intra.cu, kda_scan.cu).
+// Individual stages (kda_intra.cu, kda_scan.cu, kda_decode.cu).
 cudaError_t launch_intra(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_scan(const FwdParams& p, int groups, cudaStream_t s);
+cudaError_t launch_decode(const FwdParams& p, cudaStream_t s);
 int scan_groups(int N, int H, int num_sms);
 
 }  // namespace kda

@@ -1,4 +1,4 @@
-// State scan of the chunkwise KDA forward: one CTA per (sequence, head, block of
+// State scan of the chunkwise KDA forward: one CTA per (long sequence, head, block of
 // VS = 8*NT value rows of the state), walking the sequence's chunks in order.
 //
 // Per chunk, with the incoming state S (VS rows x K):
@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_scan_mma(FwdParams p) {
     uint64_t* sready = full + 2 * kStages;                          // [2]
     uint64_t* sfree = sready + 2;                                   // [2]
 
-    const int n = blockIdx.x;
+    const int n = p.long_list ? p.long_list[blockIdx.x] : (int)blockIdx.x;
     const int h = blockIdx.y;
     const int v0 = blockIdx.z * VS;  // first value row of this CTA
     const int tid = threadIdx.x;
@@ -416,7 +416,9 @@ cudaError_t launch_scan_nt(const FwdParams& p, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         configured |= 1u << dev;
     }
-    dim3 grid((unsigned)p.N, (unsigned)p.H, (unsigned)(D / L::VS));
+    const int n_seq = p.long_list ? p.n_long : p.N;
+    if (n_seq <= 0) return cudaSuccess;
+    dim3 grid((unsigned)n_seq, (unsigned)p.H, (unsigned)(D / L::VS));
     kda_scan_mma<NT><<<grid, kThreads, L::kTotal, s>>>(p);
     return cudaGetLastError();
 }

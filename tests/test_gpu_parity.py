@@ -38,6 +38,9 @@ CASES = [
     ([300, 5, 64], 2, torch.bfloat16, 64),
     ([77, 0, 191, 2], 2, torch.float16, 0),
     ([1] * 17 + [90], 2, torch.bfloat16, 0),
+    # around the token-by-token / chunked split (at most 8 tokens: token by token)
+    ([8, 9, 1, 0, 7, 2, 64, 3], 2, torch.float32, 32),
+    ([3] * 5 + [1] * 5 + [8], 3, torch.float16, 0),
 ]
 
 
