@@ -64,7 +64,7 @@ constexpr int kV = 65536;      // v bf16 -> b v fp16 -> u (in place)
 constexpr int kLq32 = 81920;   // q^ P fp32 [64][128]; later u for the store ([8][64][16])
 constexpr int kLk32 = 114688;  // k^ P fp32 [64][128]
 constexpr int kRd32 = 147456;  // k^ / P fp32 [64][128]; later A_qk, -A_kk, A_kk diag, T_II
-constexpr int kLQ = 180224;    // q^ P fp16, rows 16..63 ([48][128]); later X -> w ([64][128])
+constexpr int kLQ = 180224;    // q^ P fp16, rows 16..63 ([48][128]); later w ([64][128]) for the store
 constexpr int kLK = 192512;    // k^ P fp16, rows 16..63 ([48][128])
 constexpr int kRO = 204800;    // k^ E_B/P fp16, rows 0..63 ([64][128])
 constexpr int kSc = 221184;    // beta[64] | NS [16][16] | F1 [4][128] | HT [4][2][128] (fp32) | E_1, E_2
@@ -166,8 +166,8 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
     auto item_len = [&](int it, int t0) { return min(C, p.cu[p.chunk_seq[it / H] + 1] - t0); };
 
     // A tile results of one warp into place: sel 0 = A_qk (to the staging tile,
-    // j <= i), sel 1 = A_kk (diagonal block in fp32 with j < i, off-diagonal
-    // blocks negated in fp16).
+    // j <= i), sel 1 = A_kk (diagonal block in fp32, column-major, with j < i;
+    // off-diagonal blocks negated in fp16).
     auto put = [&](int sel, int tI, int tJ, const float (&acc)[2][4]) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
@@ -182,11 +182,11 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
                         if (j + 1 > i) x1 = 0.f;
                     }
                     *reinterpret_cast<uint32_t*>(smem + kAqkStage + sw64_off(i, j)) = pack_half2(x0, x1);
-                } else if (tI == tJ) {
+                } else if (tI == tJ) {  // column-major: d[j][i] = A_kk[i][j]
                     float* d = reinterpret_cast<float*>(smem + kAkd) + tI * 256;
                     const float bi = beta[i];
-                    *reinterpret_cast<float2*>(d + (i & 15) * 16 + (j & 15)) =
-                        make_float2((j >= i) ? 0.f : bi * x0, (j + 1 >= i) ? 0.f : bi * x1);
+                    d[(j & 15) * 16 + (i & 15)] = (j >= i) ? 0.f : bi * x0;
+                    d[((j + 1) & 15) * 16 + (i & 15)] = (j + 1 >= i) ? 0.f : bi * x1;
                 } else {
                     const float bi = -beta[i];
                     *reinterpret_cast<uint32_t*>(smem + kNAk + sw64_off(i, j)) =
@@ -468,7 +468,7 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
                 mma_f16(acc[1][1], ak, b4[2], b4[3]);
             }
         }
-        __syncthreads();  // the operand tiles are consumed (k^ P stays for X)
+        __syncthreads();  // the operand tiles are consumed (k^ P stays for the solve)
 
         // beta of the next item (its chunk metadata has landed by now; len_next <=
         // 64, so only the first 64 threads load)
@@ -476,29 +476,32 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
                                                       : 0.f;
 
         // ---- results into place; then the k-left diagonal warps invert their
-        //      16x16 block T_II = (I + A_II)^{-1} (registers, 16 lanes), and
-        //      warps 8-15 form X = b k^ e^G (fp16, in the LQ area) --------------
+        //      16x16 block T_II = (I + A_II)^{-1} (registers, 16 lanes) ----------
         if (warp < 8) {
             const int I = warp >> 1;
             put(warp & 1, I, I, acc[0]);
             if (warp & 1) {
                 __syncwarp();
                 if (lane < 16) {
+                    // column col of T by forward substitution, column by column of
+                    // A: once t[j] is final, every later row takes its update from
+                    // it (independent updates, so the dependent chain is 16 long)
                     const int col = lane;
                     const float* Ad = reinterpret_cast<const float*>(smem + kAkd) + I * 256;
                     float t[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float arow[16];
+                    for (int i = 0; i < 16; ++i) t[i] = (i == col) ? 1.f : 0.f;
 #pragma unroll
-                        for (int j4 = 0; j4 < 4; ++j4)
-                            if (4 * j4 < i)
-                                *reinterpret_cast<float4*>(arow + 4 * j4) =
-                                    *reinterpret_cast<const float4*>(Ad + i * 16 + 4 * j4);
-                        float s = (i == col) ? 1.f : 0.f;
+                    for (int j = 0; j < 15; ++j) {
+                        float acol[16];
 #pragma unroll
-                        for (int j = 0; j < i; ++j) s -= arow[j] * t[j];
-                        t[i] = s;  // zero above the diagonal since t[j] = 0 for j < col
+                        for (int i4 = 0; i4 < 4; ++i4)
+                            if (4 * i4 + 3 > j)
+                                *reinterpret_cast<float4*>(acol + 4 * i4) =
+                                    *reinterpret_cast<const float4*>(Ad + j * 16 + 4 * i4);
+                        const float tj = t[j];
+#pragma unroll
+                        for (int i = j + 1; i < 16; ++i) t[i] = fmaf(-acol[i], tj, t[i]);
                     }
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
@@ -512,31 +515,6 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
                 pair_of(warp - 8, tI, tJ);
                 put(0, tI, tJ, acc[0]);
                 put(1, tI, tJ, acc[1]);
-            }
-            const int t2 = tid - 256;
-            const int r = (lane & 7) + 8 * (t2 >> 5);  // 8 consecutive lanes: 8 rows
-            const int cg = lane >> 3;                   // 32-channel group
-            const int Br = r >> 4;
-            const float bt = beta[r];
-#pragma unroll
-            for (int pass = 0; pass < 2; ++pass) {
-                const int c0 = 32 * cg + 16 * pass;
-                float lk[16], f1[16];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    *reinterpret_cast<float4*>(lk + 4 * j) =
-                        *reinterpret_cast<const float4*>(smem + kLk32 + sw128f_off(r, c0 + 4 * j, 64));
-                    *reinterpret_cast<float4*>(f1 + 4 * j) =
-                        *reinterpret_cast<const float4*>(F1 + Br * 128 + c0 + 4 * j);
-                }
-                uint32_t ox[8];
-#pragma unroll
-                for (int e2 = 0; e2 < 8; ++e2)
-                    ox[e2] = pack_half2(bt * lk[2 * e2] * f1[2 * e2], bt * lk[2 * e2 + 1] * f1[2 * e2 + 1]);
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    *reinterpret_cast<uint4*>(smem + kLQ + sw128_off(r, c0 + 8 * j, 64)) =
-                        make_uint4(ox[4 * j], ox[4 * j + 1], ox[4 * j + 2], ox[4 * j + 3]);
             }
         }
         fence_proxy_async();  // the A_qk staging tile is read by the bulk store
@@ -553,9 +531,11 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
         //        R_I^T = X_I^T - sum_{J<I} W_J^T A_IJ^T,   W_I^T = R_I^T T_II^T
         //      with the columns as the MMA rows.  An m16n8k16 accumulator holding
         //      (column, row pair) is exactly the A fragment of the next product,
-        //      so R_I^T and the W_J^T feed the MMAs directly; X_I^T enters as
-        //      X_I^T times the identity.  W goes out through stmatrix.trans into
-        //      the staging tiles (w over X in the LQ area, u in the q^P area).
+        //      so R_I^T and the W_J^T feed the MMAs directly.  X = b k^ e^G enters
+        //      in fp32, formed per element from k^ P (still in its tile), b and the
+        //      block prefix F1; Y = b v enters as Y_I^T times the identity.  W goes
+        //      out through stmatrix.trans into the staging tiles (w in the LQ area,
+        //      u in the q^P area).
         {
             const bool isu = warp >= 8;
             const int n0 = 16 * (warp & 7);
@@ -569,12 +549,25 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
 #pragma unroll
             for (int I = 0; I < 4; ++I) {
                 float acc[2][4] = {};
-                {
+                if (isu) {
                     uint32_t xa[4];
                     ldsm_x4_t(xb + sw128_off(16 * I + 8 * (mi >> 1) + rr, n0 + 8 * (mi & 1), 64), xa[0],
                               xa[1], xa[2], xa[3]);
                     mma_f16(acc[0], xa, id, 0u);
                     mma_f16(acc[1], xa, 0u, id);
+                } else {
+                    // accumulator element (column n0 + g + 8(e >> 1), row 16I + 8nt + 2tq + (e & 1))
+                    const float f1a = F1[I * 128 + n0 + g8], f1b = F1[I * 128 + n0 + g8 + 8];
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int row = 16 * I + 8 * nt + 2 * tq + (e & 1);
+                            const int col = n0 + g8 + 8 * (e >> 1);
+                            acc[nt][e] = beta[row] * ((e >> 1) ? f1b : f1a) *
+                                         *reinterpret_cast<const float*>(smem + kLk32 +
+                                                                         sw128f_off(row, col, 64));
+                        }
                 }
 #pragma unroll
                 for (int J = 0; J < I; ++J) {
@@ -598,7 +591,7 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
                 wf[I][1] = pack_half2(wv[0][2], wv[0][3]);
                 wf[I][2] = pack_half2(wv[1][0], wv[1][1]);
                 wf[I][3] = pack_half2(wv[1][2], wv[1][3]);
-                __syncwarp();  // X_I of these columns is read: W_I may overwrite it
+                __syncwarp();  // Y_I of these columns is read: W_I may overwrite it
                 const int row = 16 * I + 8 * (mi >> 1) + rr;
                 if (isu)
                     stsm_x4_t(ub + row * 32 + 16 * (mi & 1), wf[I][0], wf[I][1], wf[I][2], wf[I][3]);
