@@ -134,6 +134,49 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# Ranks (N > 1: one process per GPU; every rank runs an independent replica)
+# ---------------------------------------------------------------------------
+
+class Ranks:
+    """Process-group bookkeeping for the timed region: a barrier on both sides
+    and the maximum of the per-rank times.  One rank: no process group, and
+    both are local.  `backend` is "nccl" on the GPUs; the CPU tests use "gloo"."""
+
+    def __init__(self, rank, world, backend="nccl", device=None):
+        import torch
+        self.rank, self.world, self.device = rank, world, device
+        self.dist = None
+        if world > 1:
+            import torch.distributed as dist
+            if backend == "nccl":
+                dist.init_process_group("nccl", device_id=device)
+            else:
+                dist.init_process_group(backend)
+            self.dist = dist
+        self._cuda = device is not None and torch.device(device).type == "cuda"
+
+    def barrier(self):
+        import torch
+        if self.dist is not None:
+            self.dist.barrier()
+        if self._cuda:
+            torch.cuda.synchronize(self.device)
+
+    def max_over_ranks(self, x):
+        import torch
+        if self.dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=self.device if self._cuda else "cpu")
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+            self.dist = None
+
+
+# ---------------------------------------------------------------------------
 # Our implementation
 # ---------------------------------------------------------------------------
 
@@ -144,10 +187,7 @@ def run_ours(args, rank, world):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
+    ranks = Ranks(rank, world, "nccl", dev)
     kda.load_library()
 
     w = wl.WORKLOADS[args.workload]()
@@ -168,17 +208,8 @@ def run_ours(args, rank, world):
                       has_initial_state=hs, out=out, lower_bound=w.lower_bound,
                       cu_seqlens_cpu=w.cu_seqlens, workspace=ws)
 
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-        torch.cuda.synchronize(dev)
-
-    def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    barrier = ranks.barrier
+    max_over_ranks = ranks.max_over_ranks
 
     for _ in range(args.warmup):
         step()
@@ -258,8 +289,7 @@ def run_ours(args, rank, world):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     if rank != 0:
-        if dist is not None:
-            dist.destroy_process_group()
+        ranks.close()
         return
 
     hbm, tf_burst, tf_sust, src = peaks()
@@ -308,8 +338,7 @@ def run_ours(args, rank, world):
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(line))
-    if dist is not None:
-        dist.destroy_process_group()
+    ranks.close()
 
 
 def load_traffic(kernel, workload):
