@@ -40,6 +40,13 @@ FALLBACK_BF16_TFLOPS = 1900.0
 BYTES_PER_TOKHEAD = 1540
 INTRA_BYTES_PER_TOKHEAD = 1284   # what the chunk-parallel kernel must read
 SCAN_BYTES_PER_TOKHEAD = 256     # what the scan must write (+ state bytes)
+RAW_BF16_SAVING = 258            # raw gate (128 x 2 B) and beta (2 B) read as bf16
+
+
+def raw_saving(w):
+    """Bytes per token-head the raw bf16 gate and beta save over fp32."""
+    import torch
+    return RAW_BF16_SAVING if w.g_raw.dtype == torch.bfloat16 else 0
 # Algorithmic FLOPs per token-head at the reference chunk of 64:
 # 2 * (5 C^2 d + 3 C d^2) / C with d = 128.
 FLOP_PER_TOKHEAD = 2 * (5 * 64 * 64 * 128 + 3 * 64 * 128 * 128) // 64
@@ -293,11 +300,11 @@ def run_ours(args, rank, world):
         return
 
     hbm, tf_burst, tf_sust, src = peaks()
-    bytes_alg = BYTES_PER_TOKHEAD * T * H + state_bytes(w)
+    bytes_alg = (BYTES_PER_TOKHEAD - raw_saving(w)) * T * H + state_bytes(w)
     flops_alg = FLOP_PER_TOKHEAD * T * H
     t_roof = max(bytes_alg / (hbm * 1e9), flops_alg / (tf_burst * 1e12))
     dom = max(kavg, key=kavg.get)
-    dom_bytes = (INTRA_BYTES_PER_TOKHEAD * T * H if dom == "kda_intra"
+    dom_bytes = ((INTRA_BYTES_PER_TOKHEAD - raw_saving(w)) * T * H if dom == "kda_intra"
                  else SCAN_BYTES_PER_TOKHEAD * T * H + state_bytes(w))
     dom_gbs = dom_bytes / (kavg[dom] / 1e3) / 1e9
     traffic = load_traffic(dom, args.workload)

@@ -143,6 +143,25 @@ KDA_API int kda_chunk_fwd(const void* q, const void* k, const void* v,
                   void* workspace, size_t workspace_bytes, kda_stream_t stream);
 
 /*
+ * kda_chunk_fwd_raw_bf16 — kda_chunk_fwd with the raw gate and raw beta in
+ * bf16 (g_raw device bf16 [total_tokens][num_heads][128], beta_raw device bf16
+ * [total_tokens][num_heads], 2-byte aligned); every other argument, the
+ * arithmetic (fp32 from the up-converted values) and the error codes are those
+ * of kda_chunk_fwd.  Reading 2 bytes per raw value instead of 4 cuts the
+ * input bytes by 258 per token-head.  The pages run the fused prep on raw-bf16
+ * as well as fp32 beta (ROCm/aiter PR #4741, "Accuracy": the unit tests cover
+ * raw-bf16 vs fp32 beta).
+ */
+KDA_API int kda_chunk_fwd_raw_bf16(const void* q, const void* k, const void* v,
+                  const void* g_raw, const void* beta_raw,
+                  const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                  int32_t num_seqs, int64_t total_tokens, int32_t num_heads,
+                  void* state_cache, int64_t state_stride0, int32_t num_slots,
+                  const int32_t* state_indices, const uint8_t* has_initial_state,
+                  void* out, float lower_bound, int state_dtype,
+                  void* workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/*
  * kda_chunk_fwd_dense — the same forward with dense per-sequence states.
  *
  *   initial_state     device [num_seqs][num_heads][128][128] of state_dtype,

@@ -35,7 +35,7 @@ STATE_DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 EXPORTED = (
     "kda_chunk_size", "kda_workspace_size", "kda_chunk_fwd", "kda_chunk_fwd_dense",
     "kda_plan_chunks", "kda_last_error", "kda_release_cache", "kda_cache_entries",
-    "kda_set_kernel_timing", "kda_kernel_times", "kda_kernel_name",
+    "kda_set_kernel_timing", "kda_kernel_times", "kda_kernel_name", "kda_chunk_fwd_raw_bf16",
     "kda_chunk_fwd_noalloc",
 )
 
@@ -83,6 +83,8 @@ def load_library(path: str = LIB_PATH):
         _vp, ctypes.c_float, ctypes.c_int,  # out lower_bound state_dtype
         _vp, ctypes.c_size_t, _vp,      # workspace bytes stream
     ]
+    lib.kda_chunk_fwd_raw_bf16.restype = ctypes.c_int
+    lib.kda_chunk_fwd_raw_bf16.argtypes = list(lib.kda_chunk_fwd.argtypes)
     lib.kda_chunk_fwd_dense.restype = ctypes.c_int
     lib.kda_chunk_fwd_dense.argtypes = [
         _vp, _vp, _vp, _vp, _vp,
@@ -201,15 +203,17 @@ def _workspace(workspace, T, N, H, device):
     return workspace
 
 
-def _common(q, k, v, g_raw, beta_raw, cu_seqlens):
+def _common(q, k, v, g_raw, beta_raw, cu_seqlens, raw_dtypes=(torch.float32,)):
     if q.dim() == 4:
         if q.shape[0] != 1:
             raise ValueError("packed varlen input must have batch dim 1")
     _flat(q, "q", torch.bfloat16)
     _flat(k, "k", torch.bfloat16)
     _flat(v, "v", torch.bfloat16)
-    _flat(g_raw, "g_raw", torch.float32)
-    _flat(beta_raw, "beta_raw", torch.float32)
+    if g_raw.dtype not in raw_dtypes or beta_raw.dtype != g_raw.dtype:
+        raise TypeError(f"g_raw and beta_raw must share a dtype among {raw_dtypes}")
+    _flat(g_raw, "g_raw", g_raw.dtype)
+    _flat(beta_raw, "beta_raw", beta_raw.dtype)
     T, H, D = q.shape[-3], q.shape[-2], q.shape[-1]
     if D != 128 or tuple(k.shape[-3:]) != (T, H, D) or tuple(v.shape[-3:]) != (T, H, D):
         raise ValueError("q, k, v must be [1, T, H, 128]")
@@ -223,10 +227,12 @@ def _common(q, k, v, g_raw, beta_raw, cu_seqlens):
 def chunk_fwd(q, k, v, g_raw, beta_raw, cu_seqlens, *, state_cache, state_indices,
               has_initial_state, out, lower_bound: float = -5.0, cu_seqlens_cpu=None,
               workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Paged-pool forward (``kda_chunk_fwd``).  Writes ``out`` and the selected
-    pool slots in place and returns ``out``."""
+    """Paged-pool forward (``kda_chunk_fwd``, or ``kda_chunk_fwd_raw_bf16`` when
+    g_raw and beta_raw are bf16).  Writes ``out`` and the selected pool slots in
+    place and returns ``out``."""
     lib = load_library()
-    T, H, N = _common(q, k, v, g_raw, beta_raw, cu_seqlens)
+    T, H, N = _common(q, k, v, g_raw, beta_raw, cu_seqlens,
+                      raw_dtypes=(torch.float32, torch.bfloat16))
     _flat(out, "out", torch.bfloat16)
     if tuple(out.shape) != tuple(v.shape):
         raise ValueError("out must have the shape of v")
@@ -246,7 +252,8 @@ def chunk_fwd(q, k, v, g_raw, beta_raw, cu_seqlens, *, state_cache, state_indice
     host = _host_bounds(cu_seqlens_cpu)
     ws = _workspace(workspace, T, N, H, q.device)
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
-    rc = lib.kda_chunk_fwd(
+    fn = lib.kda_chunk_fwd_raw_bf16 if g_raw.dtype == torch.bfloat16 else lib.kda_chunk_fwd
+    rc = fn(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw),
         _ptr(cu_seqlens), _ptr(host), N, T, H,
         _ptr(state_cache), state_cache.stride(0), state_cache.shape[0],

@@ -408,11 +408,11 @@ struct StateArgs {
     const uint8_t* has_init;
 };
 
-int run_forward(const void* q, const void* k, const void* v, const float* g_raw,
-                const float* beta_raw, const int32_t* cu_dev, const int32_t* cu_host,
-                int32_t N, int64_t T, int32_t H, const StateArgs& st, int state_dtype,
-                void* out, float lower_bound, void* workspace, size_t workspace_bytes,
-                cudaStream_t stream) {
+int run_forward(const void* q, const void* k, const void* v, const void* g_raw,
+                const void* beta_raw, int raw_bf16, const int32_t* cu_dev,
+                const int32_t* cu_host, int32_t N, int64_t T, int32_t H, const StateArgs& st,
+                int state_dtype, void* out, float lower_bound, void* workspace,
+                size_t workspace_bytes, cudaStream_t stream) {
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     cudaError_t e = cudaStreamIsCapturing(stream, &cap);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
@@ -454,6 +454,7 @@ int run_forward(const void* q, const void* k, const void* v, const float* g_raw,
     p.v = static_cast<const __nv_bfloat16*>(v);
     p.g_raw = g_raw;
     p.beta_raw = beta_raw;
+    p.raw_bf16 = raw_bf16;
     p.out = static_cast<__nv_bfloat16*>(out);
     p.H = H;
     p.N = N;
@@ -500,10 +501,11 @@ int run_forward(const void* q, const void* k, const void* v, const float* g_raw,
     return KDA_OK;
 }
 
-int common_checks(const void* q, const void* k, const void* v, const float* g_raw,
-                  const float* beta_raw, const int32_t* cu_dev, const int32_t* cu_host,
-                  int32_t N, int64_t T, int32_t H, void* out, float lower_bound,
-                  int state_dtype, void* workspace, size_t workspace_bytes) {
+int common_checks(const void* q, const void* k, const void* v, const void* g_raw,
+                  const void* beta_raw, int raw_bf16, const int32_t* cu_dev,
+                  const int32_t* cu_host, int32_t N, int64_t T, int32_t H, void* out,
+                  float lower_bound, int state_dtype, void* workspace,
+                  size_t workspace_bytes) {
     if (N < 0) return fail(KDA_ERR_INVALID_ARG, "num_seqs = %d < 0", N);
     if (T < 0) return fail(KDA_ERR_INVALID_ARG, "total_tokens = %lld < 0", (long long)T);
     if (T > INT32_MAX - kChunk)
@@ -526,11 +528,14 @@ int common_checks(const void* q, const void* k, const void* v, const float* g_ra
         for (int i = 0; i < 5; ++i)
             if (!aligned(p16[i], 16))
                 return fail(KDA_ERR_UNSUPPORTED, "%s is not 16-byte aligned", n16[i]);
-        if (!aligned(beta_raw, 4)) return fail(KDA_ERR_UNSUPPORTED, "beta_raw is not 4-byte aligned");
+        const size_t relt = raw_bf16 ? 2 : 4;  // bytes per raw gate / beta element
+        if (!aligned(beta_raw, relt))
+            return fail(KDA_ERR_UNSUPPORTED, "beta_raw is not %zu-byte aligned", relt);
         const size_t act = (size_t)T * H * kD * 2;
         Range ro = rng("out", out, act);
         Range ins[] = {rng("q", q, act), rng("k", k, act), rng("v", v, act),
-                       rng("g_raw", g_raw, act * 2), rng("beta_raw", beta_raw, (size_t)T * H * 4)};
+                       rng("g_raw", g_raw, act / 2 * relt),
+                       rng("beta_raw", beta_raw, (size_t)T * H * relt)};
         for (auto& r : ins)
             if (overlaps(ro, r)) return fail(KDA_ERR_INVALID_ARG, "out overlaps %s", r.name);
     }
@@ -588,17 +593,21 @@ int kda_plan_chunks(const int32_t* cu, int32_t N, int32_t chunk_size, int32_t* c
     return KDA_OK;
 }
 
-int kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g_raw,
-                  const float* beta_raw, const int32_t* cu_seqlens,
+}  // extern "C"
+
+namespace {
+// The paged forward for either raw gate / beta type (raw_bf16: bf16, else fp32).
+int paged_forward(const void* q, const void* k, const void* v, const void* g_raw,
+                  const void* beta_raw, int raw_bf16, const int32_t* cu_seqlens,
                   const int32_t* cu_seqlens_host, int32_t num_seqs, int64_t total_tokens,
                   int32_t num_heads, void* state_cache, int64_t state_stride0,
                   int32_t num_slots, const int32_t* state_indices,
                   const uint8_t* has_initial_state, void* out, float lower_bound,
                   int state_dtype, void* workspace, size_t workspace_bytes,
                   kda_stream_t stream) {
-    int rc = common_checks(q, k, v, g_raw, beta_raw, cu_seqlens, cu_seqlens_host, num_seqs,
-                           total_tokens, num_heads, out, lower_bound, state_dtype, workspace,
-                           workspace_bytes);
+    int rc = common_checks(q, k, v, g_raw, beta_raw, raw_bf16, cu_seqlens, cu_seqlens_host,
+                           num_seqs, total_tokens, num_heads, out, lower_bound, state_dtype,
+                           workspace, workspace_bytes);
     if (rc != KDA_OK) return rc;
     const int64_t plane = (int64_t)num_heads * kD * kD;
     if (num_seqs > 0) {
@@ -620,18 +629,50 @@ int kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g_ra
         const size_t pool_bytes = ((size_t)(num_slots - 1) * state_stride0 + plane) * elt;
         Range rp = rng("state_cache", state_cache, pool_bytes);
         const size_t act = (size_t)total_tokens * num_heads * kD * 2;
+        const size_t relt = raw_bf16 ? 2 : 4;
         Range others[] = {rng("q", q, act), rng("k", k, act), rng("v", v, act),
-                          rng("g_raw", g_raw, act * 2),
-                          rng("beta_raw", beta_raw, (size_t)total_tokens * num_heads * 4),
+                          rng("g_raw", g_raw, act / 2 * relt),
+                          rng("beta_raw", beta_raw, (size_t)total_tokens * num_heads * relt),
                           rng("out", out, act)};
         for (auto& r : others)
             if (overlaps(rp, r)) return fail(KDA_ERR_INVALID_ARG, "state_cache overlaps %s", r.name);
     }
     StateArgs st{state_cache, state_cache, state_stride0, state_stride0,
                  state_indices, state_indices, has_initial_state};
-    return run_forward(q, k, v, g_raw, beta_raw, cu_seqlens, cu_seqlens_host, num_seqs,
-                       total_tokens, num_heads, st, state_dtype, out, lower_bound, workspace,
-                       workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+    return run_forward(q, k, v, g_raw, beta_raw, raw_bf16, cu_seqlens, cu_seqlens_host,
+                       num_seqs, total_tokens, num_heads, st, state_dtype, out, lower_bound,
+                       workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+}  // namespace
+
+extern "C" {
+
+int kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g_raw,
+                  const float* beta_raw, const int32_t* cu_seqlens,
+                  const int32_t* cu_seqlens_host, int32_t num_seqs, int64_t total_tokens,
+                  int32_t num_heads, void* state_cache, int64_t state_stride0,
+                  int32_t num_slots, const int32_t* state_indices,
+                  const uint8_t* has_initial_state, void* out, float lower_bound,
+                  int state_dtype, void* workspace, size_t workspace_bytes,
+                  kda_stream_t stream) {
+    return paged_forward(q, k, v, g_raw, beta_raw, 0, cu_seqlens, cu_seqlens_host, num_seqs,
+                         total_tokens, num_heads, state_cache, state_stride0, num_slots,
+                         state_indices, has_initial_state, out, lower_bound, state_dtype,
+                         workspace, workspace_bytes, stream);
+}
+
+int kda_chunk_fwd_raw_bf16(const void* q, const void* k, const void* v, const void* g_raw,
+                           const void* beta_raw, const int32_t* cu_seqlens,
+                           const int32_t* cu_seqlens_host, int32_t num_seqs,
+                           int64_t total_tokens, int32_t num_heads, void* state_cache,
+                           int64_t state_stride0, int32_t num_slots,
+                           const int32_t* state_indices, const uint8_t* has_initial_state,
+                           void* out, float lower_bound, int state_dtype, void* workspace,
+                           size_t workspace_bytes, kda_stream_t stream) {
+    return paged_forward(q, k, v, g_raw, beta_raw, 1, cu_seqlens, cu_seqlens_host, num_seqs,
+                         total_tokens, num_heads, state_cache, state_stride0, num_slots,
+                         state_indices, has_initial_state, out, lower_bound, state_dtype,
+                         workspace, workspace_bytes, stream);
 }
 
 int kda_chunk_fwd_dense(const void* q, const void* k, const void* v, const float* g_raw,
@@ -641,7 +682,7 @@ int kda_chunk_fwd_dense(const void* q, const void* k, const void* v, const float
                         const uint8_t* has_initial_state, void* final_state, int state_dtype,
                         void* out, float lower_bound, void* workspace,
                         size_t workspace_bytes, kda_stream_t stream) {
-    int rc = common_checks(q, k, v, g_raw, beta_raw, cu_seqlens, cu_seqlens_host, num_seqs,
+    int rc = common_checks(q, k, v, g_raw, beta_raw, 0, cu_seqlens, cu_seqlens_host, num_seqs,
                            total_tokens, num_heads, out, lower_bound, state_dtype, workspace,
                            workspace_bytes);
     if (rc != KDA_OK) return rc;
@@ -666,7 +707,7 @@ int kda_chunk_fwd_dense(const void* q, const void* k, const void* v, const float
             return fail(KDA_ERR_INVALID_ARG, "final_state partially overlaps initial_state");
     }
     StateArgs st{initial_state, final_state, plane, plane, nullptr, nullptr, has_initial_state};
-    return run_forward(q, k, v, g_raw, beta_raw, cu_seqlens, cu_seqlens_host, num_seqs,
+    return run_forward(q, k, v, g_raw, beta_raw, 0, cu_seqlens, cu_seqlens_host, num_seqs,
                        total_tokens, num_heads, st, state_dtype, out, lower_bound, workspace,
                        workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -846,7 +887,7 @@ extern "C" int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v
     void* scratch = nullptr;
     int rc = noalloc_scratch(&scratch);
     if (rc != KDA_OK) return rc;
-    rc = common_checks(q, k, v, g_raw, beta_raw, cu_seqlens, cu_seqlens_host, num_seqs,
+    rc = common_checks(q, k, v, g_raw, beta_raw, 0, cu_seqlens, cu_seqlens_host, num_seqs,
                        total_tokens, num_heads, out, lower_bound, state_dtype, scratch,
                        (size_t)KDA_NOALLOC_SCRATCH_BYTES);
     if (rc != KDA_OK) return rc;

@@ -125,11 +125,12 @@ __global__ void __launch_bounds__(kDecThreads) kda_decode(FwdParams p) {
         // the token's q^, k^ and a, one key per thread
         float qv = 0.f, kv = 0.f;
         if (tid == 0)
-            s_beta = __fdividef(1.f, 1.f + __expf(-p.beta_raw[(size_t)(tok0 + t) * H + h]));
+            s_beta = __fdividef(
+                1.f, 1.f + __expf(-load_raw(p.beta_raw, p.raw_bf16, (size_t)(tok0 + t) * H + h)));
         {
             qv = __bfloat162float(p.q[row + tid]);
             kv = __bfloat162float(p.k[row + tid]);
-            const float gv = p.g_raw[row + tid];
+            const float gv = load_raw(p.g_raw, p.raw_bf16, row + tid);
             s_a[tid] = __expf(lb * __fdividef(1.f, 1.f + __expf(-gv)));
             float sq = qv * qv, sk = kv * kv;
 #pragma unroll

@@ -43,8 +43,9 @@ struct FwdParams {
     const __nv_bfloat16* q;
     const __nv_bfloat16* k;
     const __nv_bfloat16* v;
-    const float* g_raw;
-    const float* beta_raw;
+    const void* g_raw;      // [T][H][128], fp32, or bf16 when raw_bf16
+    const void* beta_raw;   // [T][H], fp32, or bf16 when raw_bf16
+    int raw_bf16;
     __nv_bfloat16* out;
     int H;
     int N;
@@ -79,6 +80,12 @@ struct FwdParams {
     const uint8_t* has_init;  // nullptr: every sequence has one iff st_in != nullptr
     int st_dtype;             // 0 fp32, 1 bf16, 2 fp16
 };
+
+// Element i of a raw gate / beta array (fp32, or bf16 when raw_bf16 is set).
+__device__ __forceinline__ float load_raw(const void* p, int raw_bf16, size_t i) {
+    return raw_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i])
+                    : static_cast<const float*>(p)[i];
+}
 
 inline size_t workspace_bytes(int64_t max_chunks, int H) {
     return (size_t)kWsHeader + (size_t)max_chunks * (size_t)H * (size_t)kWsBytes;

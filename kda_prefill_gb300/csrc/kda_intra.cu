@@ -74,7 +74,7 @@ kda_intra_exact(FwdParams p) {
             qv = __bfloat162float(p.q[off]);
             kv = __bfloat162float(p.k[off]);
             vv = __bfloat162float(p.v[off]);
-            gv = p.lower_bound * sigmoidf_(p.g_raw[off]);
+            gv = p.lower_bound * sigmoidf_(load_raw(p.g_raw, p.raw_bf16, off));
         }
         sQ[r * P + c] = qv;
         sK[r * P + c] = kv;
@@ -82,7 +82,8 @@ kda_intra_exact(FwdParams p) {
         sG[r * P + c] = gv;
     }
     for (int r = tid; r < C; r += kIntraThreads)
-        sB[r] = (r < len) ? sigmoidf_(p.beta_raw[(size_t)(tok0 + r) * p.H + h]) : 0.f;
+        sB[r] = (r < len) ? sigmoidf_(load_raw(p.beta_raw, p.raw_bf16, (size_t)(tok0 + r) * p.H + h))
+                          : 0.f;
     __syncthreads();
 
     const int warp = tid / 32, lane = tid % 32;

@@ -59,7 +59,7 @@ constexpr int kThreads = 512;
 // Shared-memory layout (bytes).
 constexpr int kQ = 0;          // q bf16 [64][128] (TMA, swizzled halves)
 constexpr int kK = 16384;      // k bf16
-constexpr int kG = 32768;      // g_raw fp32 [64][128] (TMA, swizzled quarters)
+constexpr int kG = 32768;      // g_raw fp32 [64][128] (TMA, swizzled quarters), or bf16 (halves, 16 KB)
 constexpr int kV = 65536;      // v bf16 -> b v fp16 -> u (in place)
 constexpr int kLq32 = 81920;   // q^ P fp32 [64][128]; later u for the store ([8][64][16])
 constexpr int kLk32 = 114688;  // k^ P fp32 [64][128]
@@ -110,6 +110,9 @@ __device__ __forceinline__ void pair_of(int pi, int& I, int& J) {
     J = pi - I * (I - 1) / 2;
 }
 
+// RAW16: raw gate and beta in bf16 (the gate tile then takes 16 KB of the g
+// area, laid out like q and k) instead of fp32.
+template <bool RAW16>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -146,14 +149,19 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
     // TMA issue (one thread).
     auto issue_inputs = [&](int it, int t0) {
         const int h = it % H;
-        mbar_arrive_expect_tx(&bar[0], 65536);
+        mbar_arrive_expect_tx(&bar[0], RAW16 ? 49152 : 65536);
         tma_load_3d(smem + kQ, &maps.q, &bar[0], 0, h, t0);
         tma_load_3d(smem + kQ + 8192, &maps.q, &bar[0], 64, h, t0);
         tma_load_3d(smem + kK, &maps.k, &bar[0], 0, h, t0);
         tma_load_3d(smem + kK + 8192, &maps.k, &bar[0], 64, h, t0);
+        if (RAW16) {
+            tma_load_3d(smem + kG, &maps.g, &bar[0], 0, h, t0);
+            tma_load_3d(smem + kG + 8192, &maps.g, &bar[0], 64, h, t0);
+        } else {
 #pragma unroll
-        for (int qt = 0; qt < 4; ++qt)
-            tma_load_3d(smem + kG + qt * 8192, &maps.g, &bar[0], 32 * qt, h, t0);
+            for (int qt = 0; qt < 4; ++qt)
+                tma_load_3d(smem + kG + qt * 8192, &maps.g, &bar[0], 32 * qt, h, t0);
+        }
     };
     auto issue_v = [&](int it, int t0) {
         const int h = it % H;
@@ -205,7 +213,7 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
             issue_inputs(first, tok_next);
             issue_v(first, tok_next);
         }
-        if (tid < len_next) braw_next = p.beta_raw[(size_t)(tok_next + tid) * H + first % H];
+        if (tid < len_next) braw_next = load_raw(p.beta_raw, RAW16, (size_t)(tok_next + tid) * H + first % H);
     }
 
     int n_local = 0;
@@ -245,7 +253,13 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int r = rb + i;
-                const float2 gr = *reinterpret_cast<const float2*>(smem + kG + sw128f_off(r, c0, 64));
+                float2 gr;
+                if (RAW16) {
+                    const uint32_t gw = *reinterpret_cast<const uint32_t*>(smem + kG + sw128_off(r, c0, 64));
+                    gr = make_float2(__uint_as_float(gw << 16), __uint_as_float(gw & 0xffff0000u));
+                } else {
+                    gr = *reinterpret_cast<const float2*>(smem + kG + sw128f_off(r, c0, 64));
+                }
                 const bool valid = r < len;
                 // sigmoid of both channels from one reciprocal: with d = 1 + e^{-g}
                 // (g clamped to [-40, 40], where sigmoid is 0 or 1 to fp32 precision,
@@ -472,8 +486,9 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
 
         // beta of the next item (its chunk metadata has landed by now; len_next <=
         // 64, so only the first 64 threads load)
-        braw_next = (nxt < n_items && tid < len_next) ? p.beta_raw[(size_t)(tok_next + tid) * H + nxt % H]
-                                                      : 0.f;
+        braw_next = (nxt < n_items && tid < len_next)
+                        ? load_raw(p.beta_raw, RAW16, (size_t)(tok_next + tid) * H + nxt % H)
+                        : 0.f;
 
         // ---- results into place; then the k-left diagonal warps invert their
         //      16x16 block T_II = (I + A_II)^{-1} (registers, 16 lanes) ----------
@@ -654,7 +669,8 @@ cudaError_t launch_intra(const FwdParams& p, cudaStream_t s) {
     if (!make_map(&maps.q, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, p.H, p.T) ||
         !make_map(&maps.k, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, p.H, p.T) ||
         !make_map(&maps.v, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, p.H, p.T) ||
-        !make_map(&maps.g, p.g_raw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32, p.H, p.T))
+        !(p.raw_bf16 ? make_map(&maps.g, p.g_raw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, p.H, p.T)
+                     : make_map(&maps.g, p.g_raw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32, p.H, p.T)))
         return cudaErrorInvalidValue;
     static unsigned configured = 0;
     static int sms[32] = {0};
@@ -662,15 +678,21 @@ cudaError_t launch_intra(const FwdParams& p, cudaStream_t s) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 32 && !(configured & (1u << dev))) {
-        e = cudaFuncSetAttribute(kda_intra_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(kda_intra_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kda_intra_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmemBytes);
         if (e != cudaSuccess) return e;
         cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
         configured |= 1u << dev;
     }
     const int n_items = p.n_chunks * p.H;
     const int grid = n_items < sms[dev < 32 ? dev : 0] ? n_items : sms[dev < 32 ? dev : 0];
-    kda_intra_tc<<<grid > 0 ? grid : 1, kThreads, kSmemBytes, s>>>(maps, p);
+    if (p.raw_bf16)
+        kda_intra_tc<true><<<grid > 0 ? grid : 1, kThreads, kSmemBytes, s>>>(maps, p);
+    else
+        kda_intra_tc<false><<<grid > 0 ? grid : 1, kThreads, kSmemBytes, s>>>(maps, p);
     return cudaGetLastError();
 }
 

@@ -81,13 +81,15 @@ def make_workload(name: str, lengths: Sequence[int], num_heads: int, *,
                   pool_std: float = 0.1, state_indices: Optional[Sequence[int]] = None,
                   has_initial_state: Optional[Sequence[int]] = None,
                   init_prob: float = 0.5, lower_bound: float = -5.0, seed: int = 0,
-                  draw_lengths=None, gate_scale: float = 1.0) -> Workload:
+                  draw_lengths=None, gate_scale: float = 1.0, raw_bf16: bool = False) -> Workload:
     """Draws one workload.
 
     ``lengths`` fixes the sequence lengths unless ``draw_lengths`` is given, in
     which case it is called with the generator first (so the lengths are part
     of the seeded stream).  ``state_indices`` defaults to a random choice of
     distinct slots, ``has_initial_state`` to Bernoulli(``init_prob``).
+    ``raw_bf16`` rounds the raw gate and beta to bf16 (RNE) after drawing them,
+    so both paths read the same values.
     """
     g = torch.Generator().manual_seed(seed)
     if draw_lengths is not None:
@@ -105,6 +107,8 @@ def make_workload(name: str, lengths: Sequence[int], num_heads: int, *,
     v = _bf16(torch.randn(1, T, H, D, generator=g))
     g_raw = torch.randn(1, T, H, D, generator=g) * gate_scale
     beta_raw = torch.randn(1, T, H, generator=g)
+    if raw_bf16:
+        g_raw, beta_raw = g_raw.to(torch.bfloat16), beta_raw.to(torch.bfloat16)
 
     plane = H * D * D
     stride0 = plane + stride_pad
@@ -167,6 +171,14 @@ def prefill_16k() -> Workload:
     return w
 
 
+def prefill_16k_raw_bf16() -> Workload:
+    """The 1 x 16384, H=12 prefill with the raw gate and beta in bf16."""
+    w = make_workload("prefill_1x16384_h12_rawbf16", [16384], 12, num_slots=64,
+                      state_indices=[0], has_initial_state=[0], seed=2, raw_bf16=True)
+    poison_unread_slots(w)
+    return w
+
+
 def _varlen_lengths(g: torch.Generator, n: int = 128, max_len: int = 2048,
                     p_empty: float = 0.05):
     empty = torch.rand(n, generator=g) < p_empty
@@ -198,6 +210,7 @@ WORKLOADS = {
     "tiny_varlen": tiny_varlen,
     "prefill_4k": prefill_4k,
     "prefill_16k": prefill_16k,
+    "prefill_16k_raw_bf16": prefill_16k_raw_bf16,
     "varlen_batch": varlen_batch,
     "mixed_bf16_pool": mixed_bf16_pool,
 }

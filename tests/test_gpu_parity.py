@@ -56,6 +56,30 @@ def test_small_parity(lengths, H, dt, pad):
     assert unselected_untouched(r, before)
 
 
+RAW_BF16_CASES = [
+    # lengths, H, pool dtype, lower_bound
+    ([1, 63, 64, 65, 130, 0, 200], 3, torch.float32, -5.0),
+    ([300, 5, 64, 1, 1], 2, torch.bfloat16, -5.0),
+    ([150, 2], 2, torch.float32, -40.0),  # the exact intra-chunk kernel
+]
+
+
+@pytest.mark.parametrize("lengths,H,dt,lb", RAW_BF16_CASES)
+def test_raw_bf16_gate_and_beta(lengths, H, dt, lb):
+    """Raw gate and beta in bf16 (kda_chunk_fwd_raw_bf16): parity with the
+    oracle on the same bf16 values, through the chunked, the exact and the
+    token-by-token kernels; unselected slots untouched."""
+    w = wl.make_workload("raw16", lengths, H, num_slots=len(lengths) + 3, pool_dtype=dt,
+                         lower_bound=lb, seed=40 + sum(lengths), raw_bf16=True)
+    assert w.g_raw.dtype == torch.bfloat16 and w.beta_raw.dtype == torch.bfloat16
+    wl.poison_unread_slots(w)
+    r = DevRun(w)
+    before = r.storage.cpu().clone()
+    r.run()
+    compare(r, tol=TOL[dt])
+    assert unselected_untouched(r, before)
+
+
 def test_saturated_gates_and_strong_bound():
     """Raw gate +8 everywhere (about 5 nats of decay per token and channel at
     lower_bound -5; 160+ nats per chunk) and, separately, lower_bound -40: no
