@@ -126,6 +126,13 @@ KDA_API size_t kda_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_
  * empty sequences) run token by token in a third kernel with the state in
  * fp32 registers.  Both compute the same recurrence; only rounding differs.
  *
+ * CUDA graph capture: a call on a capturing stream is captured when
+ * cu_seqlens_host is given and an earlier call, finished before the capture
+ * began and made on any stream, had the same bounds (their tables are then
+ * cached and the graph keeps them for the life of the process).  Otherwise it
+ * returns KDA_ERR_CAPTURE_MISS and enqueues nothing.  Captured calls record no
+ * kernel timing.
+ *
  * ROCm/aiter PR #5754, "Technical Details": state_cache fp32 V-first
  * [slots, H, V, K] with a possibly padded stride(0); int32 state_indices; bool
  * has_initial_state (false starts from zero and does not read a dirty slot);

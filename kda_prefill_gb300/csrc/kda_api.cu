@@ -235,7 +235,13 @@ class MetaCache {
             MetaEntry* m = it->second;
             m->stamp = ++clock;
             if (m->upload_stream != stream) {
+                // A global-mode capture (on this thread or another) forbids
+                // cudaEventQuery on this thread; the upload event is never part
+                // of a capture, so the thread queries it in relaxed mode.
+                cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+                cudaThreadExchangeStreamCaptureMode(&mode);
                 cudaError_t q = cudaEventQuery(m->ready);
+                cudaThreadExchangeStreamCaptureMode(&mode);
                 if (q == cudaErrorNotReady) {
                     if (capturing)
                         return fail(KDA_ERR_CAPTURE_MISS,
