@@ -54,6 +54,7 @@ struct ScanSmem {
     static constexpr int kUt = kS16 + 2 * kS16Slot;          // 2 slots x [VS][64] fp16
     static constexpr int kUtSlot = VS * 128;
     static constexpr int kBar = kUt + 2 * kUtSlot;           // mbarriers
+    static constexpr int kAbort = kBar + 96;                 // int: a state warp gave up
     static constexpr int kTotal = kBar + 128;
 };
 
@@ -85,6 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_scan_mma(FwdParams p) {
     uint64_t* empty = full + kStages;                               // [kStages]
     uint64_t* sready = full + 2 * kStages;                          // [2]
     uint64_t* sfree = sready + 2;                                   // [2]
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
 
     const int n = p.long_list ? p.long_list[blockIdx.x] : (int)blockIdx.x;
     const int h = blockIdx.y;
@@ -113,6 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_scan_mma(FwdParams p) {
         mbar_init(&sready[1], 1);
         mbar_init(&sfree[0], kOutWarps);
         mbar_init(&sfree[1], kOutWarps);
+        *abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
@@ -227,16 +230,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_scan_mma(FwdParams p) {
 
     // ======================= state warps ====================================
     const int wr = warp;  // key channels 32wr..32wr+31 of S^T
+    // The state warps meet on a named barrier twice per chunk.  A warp whose
+    // wait gave up raises the shared abort flag before the barrier; all of them
+    // read it after the same barrier, so they leave the walk together (the
+    // read's latency is hidden behind the next products, the test comes after).
     auto state_sync = [&]() { asm volatile("bar.sync 1, 128;" ::: "memory"); };
-    auto state_sync_or = [&](bool flag) -> bool {
-        uint32_t any;
-        asm volatile(
-            "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-            "bar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-            : "=r"(any)
-            : "r"((uint32_t)flag)
-            : "memory");
-        return any != 0;
+    auto state_sync_flag = [&](bool failed_here) -> int {
+        if (failed_here) *abort_flag = 1;
+        state_sync();
+        return *abort_flag;
     };
 
     const bool has_init = p.has_init ? (p.has_init[n] != 0) : (p.st_in != nullptr);
@@ -336,11 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_scan_mma(FwdParams p) {
             stsm_x4_t(ut + sw64_off(vrow, ccol), uf[2 * np][0], uf[2 * np][1], uf[2 * np + 1][0],
                       uf[2 * np + 1][1]);
         }
-        if (state_sync_or(!ok)) {  // a copy never landed: report, stop the walk
-            failed = true;
-            if (tid == 0 && p.status) atomicOr(p.status, 1);
-            break;
-        }
+        const int abort1 = state_sync_flag(!ok);  // a copy never landed (tested below)
         if (tid == 0) mbar_arrive(&sready[b]);  // S (published last step) and U of this chunk
 
         // dS^T = kg^T U for key channels 32wr..32wr+31; S = gamma S + dS
@@ -373,6 +371,11 @@ __global__ void __launch_bounds__(kThreads, 1) kda_scan_mma(FwdParams p) {
                     Sm[mt][nt][2 * hh + 1] = gk * Sm[mt][nt][2 * hh + 1] + accS[mt][nt][2 * hh + 1];
                 }
             }
+        if (abort1) {  // report, stop the walk
+            failed = true;
+            if (tid == 0 && p.status) atomicOr(p.status, 1);
+            break;
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[sg]);  // w, kg, gamma and u of this stage are read
 
@@ -382,12 +385,13 @@ __global__ void __launch_bounds__(kThreads, 1) kda_scan_mma(FwdParams p) {
         bool ok2 = true;
         if (lc >= 1) ok2 = mbar_wait(&sfree[nb], ((lc - 1) >> 1) & 1);
         if (ok2) write_s16(nb);
-        if (state_sync_or(!ok2)) {
+        const int abort2 = state_sync_flag(!ok2);
+        load_sfrag(nb);
+        if (abort2) {
             failed = true;
             if (tid == 0 && p.status) atomicOr(p.status, 1);
             break;
         }
-        load_sfrag(nb);
     }
     if (failed) return;
 
