@@ -41,6 +41,10 @@ CASES = [
     # around the token-by-token / chunked split (at most 8 tokens: token by token)
     ([8, 9, 1, 0, 7, 2, 64, 3], 2, torch.float32, 32),
     ([3] * 5 + [1] * 5 + [8], 3, torch.float16, 0),
+    # more than 2 * SMs / 8 (sequence, head) pairs on a 152-SM GPU: the scan's
+    # large-batch form (32 value rows per CTA)
+    ([70, 9, 128, 200, 65, 150, 33, 99, 64, 300] * 2, 2, torch.float32, 0),
+    ([130, 65, 10, 257, 64] * 4, 2, torch.bfloat16, 64),
 ]
 
 
