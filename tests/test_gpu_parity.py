@@ -45,6 +45,10 @@ CASES = [
     # large-batch form (32 value rows per CTA)
     ([70, 9, 128, 200, 65, 150, 33, 99, 64, 300] * 2, 2, torch.float32, 0),
     ([130, 65, 10, 257, 64] * 4, 2, torch.bfloat16, 64),
+    # many short sequences: each persistent token-by-token CTA takes several items,
+    # so its ring of state stages wraps around more than once
+    ([1] * 300 + [2, 0, 5, 8] * 20, 2, torch.bfloat16, 0),
+    ([1, 3, 0, 7] * 100 + [70], 2, torch.float32, 32),
 ]
 
 
