@@ -77,12 +77,21 @@ def peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
-def state_bytes(w):
+def state_bytes(w, only_long=False):
+    """State bytes read (sequences with an initial state) and written (every
+    sequence); with only_long, those of the sequences longer than 8 tokens (the
+    ones the chunked kernels process)."""
     import torch
     elt = torch.tensor([], dtype=w.state_pool.dtype).element_size()
     plane = w.num_heads * 128 * 128 * elt
-    reads = int(w.has_initial_state.sum())
-    return plane * reads + plane * w.num_seqs
+    sel = [n for n, ln in enumerate(w.lengths) if ln > 8] if only_long else range(w.num_seqs)
+    reads = sum(1 for n in sel if bool(w.has_initial_state[n]))
+    return plane * reads + plane * len(sel)
+
+
+def long_tokens(w):
+    """Tokens of the sequences longer than 8 tokens."""
+    return sum(ln for ln in w.lengths if ln > 8)
 
 
 # ---------------------------------------------------------------------------
@@ -256,44 +265,64 @@ def run_ours(args, rank, world):
     kda.set_kernel_timing(False)
     kavg = {n: t / max(kcalls, 1) for n, t in ktimes.items()}
 
-    # end to end through the public API with host buffers
+    # end to end through the public API with host buffers: every step uploads
+    # its inputs from pinned host memory and reads its output back.  Uploads,
+    # forwards and read-backs run on three streams over two device buffer sets,
+    # so step i + 1's upload and step i - 1's read-back overlap step i's forward
+    # (the forwards themselves stay in order: each updates the state pool).
     e2e = None
     if not args.no_e2e:
-        pin = {n: getattr(w, n).pin_memory() for n in ("q", "k", "v", "g_raw", "beta_raw")}
-        cu_h = w.cu_seqlens.pin_memory()
-        idx_h = w.state_indices.pin_memory()
-        hs_h = w.has_initial_state.pin_memory()
-        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in pin.values()) + \
-            sum(t.numel() * t.element_size() for t in (cu_h, idx_h, hs_h))
-        d2h = out_h.numel() * out_h.element_size()
+        names = ("q", "k", "v", "g_raw", "beta_raw", "cu", "idx", "hs")
+        host = dict(q=w.q, k=w.k, v=w.v, g_raw=w.g_raw, beta_raw=w.beta_raw,
+                    cu=w.cu_seqlens, idx=w.state_indices, hs=w.has_initial_state)
+        pin = {n: host[n].pin_memory() for n in names}
+        sets = [dict(q=q, k=k, v=v, g_raw=g, beta_raw=b, cu=cu, idx=idx, hs=hs, out=out)]
+        sets.append({n: torch.empty_like(t) for n, t in sets[0].items()})
+        out_h = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = out_h[0].numel() * out_h[0].element_size()
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        ev_read = [torch.cuda.Event() for _ in range(2)]
 
-        def e2e_step():
-            q.copy_(pin["q"], non_blocking=True)
-            k.copy_(pin["k"], non_blocking=True)
-            v.copy_(pin["v"], non_blocking=True)
-            g.copy_(pin["g_raw"], non_blocking=True)
-            b.copy_(pin["beta_raw"], non_blocking=True)
-            cu.copy_(cu_h, non_blocking=True)
-            idx.copy_(idx_h, non_blocking=True)
-            hs.copy_(hs_h, non_blocking=True)
-            step()
-            out_h.copy_(out, non_blocking=True)
+        def e2e_step(i):
+            j = i % 2
+            B = sets[j]
+            s_in.wait_event(ev_done[j])  # set j is free once step i - 2's forward is done
+            with torch.cuda.stream(s_in):
+                for n in names:
+                    B[n].copy_(pin[n], non_blocking=True)
+            ev_in[j].record(s_in)
+            stream.wait_event(ev_in[j])
+            stream.wait_event(ev_read[j])  # step i - 2's output has been read back
+            kda.chunk_fwd(B["q"], B["k"], B["v"], B["g_raw"], B["beta_raw"], B["cu"],
+                          state_cache=pool, state_indices=B["idx"], has_initial_state=B["hs"],
+                          out=B["out"], lower_bound=w.lower_bound, cu_seqlens_cpu=w.cu_seqlens,
+                          workspace=ws, stream=stream)
+            ev_done[j].record(stream)
+            s_out.wait_event(ev_done[j])
+            with torch.cuda.stream(s_out):
+                out_h[j].copy_(B["out"], non_blocking=True)
+            ev_read[j].record(s_out)
 
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
+        for i in range(max(1, args.warmup)):
+            e2e_step(i)
+        torch.cuda.synchronize(dev)
         barrier()
         a0 = torch.cuda.Event(enable_timing=True)
         a1 = torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        a1.record(stream)
+        a0.record(s_in)
+        for i in range(args.steps):
+            e2e_step(i)
+        a1.record(s_out)
+        torch.cuda.synchronize(dev)
         barrier()
         e2e_ms = max_over_ranks(a0.elapsed_time(a1)) / args.steps
         e2e = {"value": T * world / (e2e_ms / 1e3), "unit": UNIT,
                "us_per_call": e2e_ms * 1e3,
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "schedule": "upload, forward and read-back on three streams, two buffer sets"}
 
     if rank != 0:
         ranks.close()
@@ -304,8 +333,13 @@ def run_ours(args, rank, world):
     flops_alg = FLOP_PER_TOKHEAD * T * H
     t_roof = max(bytes_alg / (hbm * 1e9), flops_alg / (tf_burst * 1e12))
     dom = max(kavg, key=kavg.get)
-    dom_bytes = ((INTRA_BYTES_PER_TOKHEAD - raw_saving(w)) * T * H if dom == "kda_intra"
-                 else SCAN_BYTES_PER_TOKHEAD * T * H + state_bytes(w))
+    if dom == "kda_intra":
+        dom_bytes = (INTRA_BYTES_PER_TOKHEAD - raw_saving(w)) * T * H
+    elif dom == "kda_fused":  # intra + scan of the long sequences
+        dom_bytes = ((BYTES_PER_TOKHEAD - raw_saving(w)) * long_tokens(w) * H +
+                     state_bytes(w, only_long=True))
+    else:
+        dom_bytes = SCAN_BYTES_PER_TOKHEAD * T * H + state_bytes(w)
     dom_gbs = dom_bytes / (kavg[dom] / 1e3) / 1e9
     traffic = load_traffic(dom, args.workload)
 

@@ -235,9 +235,11 @@ KDA_API int kda_cache_entries(void);
  * (a few microseconds of overhead, no synchronisation).  kda_kernel_times()
  * waits for the recorded events, adds each kernel's elapsed time over the calls
  * since the last read into ms[i] (i = launch order: 0 = intra-chunk kernel,
- * 1 = state scan, 2 = token-by-token kernel for short sequences), stores the
- * number of calls in *calls, the number of kernels
- * in *count, and clears the record.  Mirrors the per-kernel split the pages
+ * 1 = state scan, 2 = the two fused in one launch, used instead of 0 and 1 when
+ * the scan's walks leave enough SMs free, 3 = token-by-token kernel for short
+ * sequences; a kernel a call did not launch adds nothing), stores the number of
+ * calls in *calls, the number of kernels (4) in *count, and clears the record.
+ * ms must hold at least 4 entries.  Mirrors the per-kernel split the pages
  * report (ROCm/aiter PR #4741, "Performance": per-kernel microseconds per
  * layer-call).  Returns KDA_OK, KDA_ERR_INVALID_ARG or KDA_ERR_CUDA.
  */

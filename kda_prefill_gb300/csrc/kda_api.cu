@@ -477,6 +477,8 @@ int run_forward(const void* q, const void* k, const void* v, const void* g_raw,
     p.n_short = m->layout.n_short;
     p.ws = ws ? ws + kda::kWsHeader : nullptr;
     p.status = ws ? reinterpret_cast<int*>(ws) : nullptr;
+    p.queue = ws ? reinterpret_cast<int*>(ws + kda::kWsQueueOff) : nullptr;
+    p.ready = ws ? reinterpret_cast<int*>(ws + kda::flags_offset(max_chunks(T, N), H)) : nullptr;
     p.st_in = st.in;
     p.st_out = st.out;
     p.st_in_stride = st.in_stride;
@@ -961,6 +963,8 @@ extern "C" int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v
     p.n_short = num_seqs - n_long;
     p.ws = base + kda::kWsHeader;
     p.status = reinterpret_cast<int*>(base);
+    p.queue = reinterpret_cast<int*>(base + kda::kWsQueueOff);
+    p.ready = reinterpret_cast<int*>(base + kda::flags_offset(bound, num_heads));
     p.st_in = state_cache;
     p.st_out = state_cache;
     p.st_in_stride = state_stride0;

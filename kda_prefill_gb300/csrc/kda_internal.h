@@ -34,9 +34,12 @@ constexpr int kWsSharedBytes = 57856;
 constexpr int kWsUOff = 57856;
 constexpr int kWsUSliceBytes = 2048;
 constexpr int kWsBytes = 74240;
-// Workspace header: one int status word (bit 0: a bounded wait gave up),
-// then the chunk blocks start at kWsHeader.
+// Workspace header: one int status word (bit 0: a bounded wait gave up) and,
+// at byte kWsQueueOff, the work counter of the fused launch; the chunk blocks
+// start at kWsHeader.  After the blocks (bounded by max_chunks * H) come the
+// fused launch's ready flags, one int per (chunk, head) block.
 constexpr int kWsHeader = 256;
+constexpr int kWsQueueOff = 64;
 
 // Everything one forward launch sequence needs.  Device pointers unless noted.
 struct FwdParams {
@@ -68,6 +71,8 @@ struct FwdParams {
 
     uint8_t* ws;   // chunk blocks (kWsBytes each)
     int* status;   // workspace header
+    int* queue;    // fused launch: work counter (workspace header)
+    int* ready;    // fused launch: per (chunk, head) block, nonzero once it is written
 
     // state (paged: st_in == st_out == pool, idx = state_indices;
     //        dense: separate bases, idx == nullptr means identity)
@@ -87,12 +92,17 @@ __device__ __forceinline__ float load_raw(const void* p, int raw_bf16, size_t i)
                     : static_cast<const float*>(p)[i];
 }
 
-inline size_t workspace_bytes(int64_t max_chunks, int H) {
+inline size_t flags_offset(int64_t max_chunks, int H) {
     return (size_t)kWsHeader + (size_t)max_chunks * (size_t)H * (size_t)kWsBytes;
+}
+inline size_t workspace_bytes(int64_t max_chunks, int H) {
+    return flags_offset(max_chunks, H) + (((size_t)max_chunks * (size_t)H * 4 + 255) & ~size_t(255));
 }
 
 // Number of kernels one forward launches, and their names (launch order).
-constexpr int kNumKernels = 3;
+// Kernel 3 is the fused intra + scan launch, which replaces kernels 0 and 1
+// when the scan's CTAs leave enough SMs free for the intra-chunk work.
+constexpr int kNumKernels = 4;
 const char* kernel_name(int i);
 
 // Enqueues the kernels of one forward on `s`.  When `marks` is non-null it
@@ -107,6 +117,12 @@ unsigned launched_kernels(const FwdParams& p);
 cudaError_t launch_intra(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_scan(const FwdParams& p, int groups, cudaStream_t s);
 cudaError_t launch_decode(const FwdParams& p, cudaStream_t s);
+// Fused intra + scan launch (kda_intra_tc.cu), used instead of the two when
+// fused_eligible(p): the walks need few enough SMs, the device takes a
+// cooperative launch of one CTA per SM, and p.ready / p.queue are set.
+bool fused_eligible(const FwdParams& p);
+cudaError_t launch_fused(const FwdParams& p, cudaStream_t s);
+int num_sms();
 int scan_groups(int N, int H, int num_sms);
 
 }  // namespace kda

@@ -44,6 +44,7 @@
 
 #include "kda_device.cuh"
 #include "kda_internal.h"
+#include "kda_scan_walk.cuh"
 
 namespace kda {
 
@@ -104,18 +105,36 @@ __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Marks a (chunk, head) block as written for the fused launch's scan walks: the
+// block's bulk stores have completed (cp.async.bulk.wait_group 0 by this
+// thread) and the CTA's other stores to it came before a CTA barrier.
+__device__ __forceinline__ void publish_ready(int* flag) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __threadfence();
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(flag), "r"(1) : "memory");
+}
+
+// Item claims of the standalone launch: item blockIdx.x, then every
+// gridDim.x-th.
+struct StaticClaims {
+    __device__ int first() { return blockIdx.x; }
+    __device__ void claim() {}
+    __device__ int next(int it) { return it + gridDim.x; }
+};
+
 // Off-diagonal block pairs in order (1,0) (2,0) (2,1) (3,0) (3,1) (3,2).
 __device__ __forceinline__ void pair_of(int pi, int& I, int& J) {
     I = pi < 1 ? 1 : (pi < 3 ? 2 : 3);
     J = pi - I * (I - 1) / 2;
 }
 
-// RAW16: raw gate and beta in bf16 (the gate tile then takes 16 KB of the g
-// area, laid out like q and k) instead of fp32.
-template <bool RAW16>
-__global__ void __launch_bounds__(kThreads, 1)
-kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
-    extern __shared__ __align__(1024) uint8_t smem[];
+// The intra-chunk items of one CTA, in the order `cl` hands them out (all
+// threads call cl.first() once and, per item, cl.claim() before and cl.next()
+// after a CTA barrier).  RAW16: raw gate and beta in bf16 (the gate tile then
+// takes 16 KB of the g area, laid out like q and k) instead of fp32.
+template <bool RAW16, class Claims>
+__device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdParams& p, uint8_t* smem,
+                                            Claims& cl) {
     float* beta = reinterpret_cast<float*>(smem + kSc);
     float* NS = beta + 64;  // [16 warps][16] row sums of squares over each warp's 64 channels
     float* F1 = NS + 256;   // [4][128] decay of the blocks before B (e^G at the block start)
@@ -203,7 +222,7 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
             }
     };
 
-    const int first = blockIdx.x;
+    const int first = cl.first();
     int tok_next = 0, len_next = 0;
     float braw_next = 0.f;
     if (first < n_items) {
@@ -216,22 +235,23 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
         if (tid < len_next) braw_next = load_raw(p.beta_raw, RAW16, (size_t)(tok_next + tid) * H + first % H);
     }
 
-    int n_local = 0;
-    for (int it = first; it < n_items; it += gridDim.x, ++n_local) {
+    int n_local = 0, prev = -1;
+    for (int it = first; it < n_items; ++n_local) {
         const int len = len_next;
         const float braw = braw_next;
         uint8_t* blk = p.ws + (size_t)it * kWsBytes;
-        const int nxt = it + gridDim.x;
-        // the next item's chunk metadata, loaded while this one runs
-        if (nxt < n_items) {
-            tok_next = item_tok(nxt);
-            len_next = item_len(nxt, tok_next);
-        }
+        cl.claim();
 
         const bool ok_in = mbar_wait(&bar[0], n_local & 1);
         if (__syncthreads_or(!ok_in)) {
             if (tid == 0 && p.status) atomicOr(p.status, 1);
             break;
+        }
+        const int nxt = cl.next(it);
+        // the next item's chunk metadata, loaded while this one runs
+        if (nxt < n_items) {
+            tok_next = item_tok(nxt);
+            len_next = item_len(nxt, tok_next);
         }
 
         // ---- decay pass, all warps: thread (block B, row half hf, channels c0,
@@ -307,8 +327,16 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
             if (tid < C) beta[tid] = (tid < len) ? __fdividef(1.f, 1.f + __expf(-braw)) : 0.f;
             // the previous item's bulk stores must have read the staging areas
             // (u in the q^P area, A_qk in the k^/P area, w in the LQ area) before
-            // part 2 rewrites them
-            if (tid == 0) bulk_wait_read_all();
+            // part 2 rewrites them; for the fused launch they must have completed,
+            // and the item is then marked written
+            if (tid == 0) {
+                if (p.ready && prev >= 0) {
+                    bulk_wait_all();
+                    publish_ready(p.ready + prev);
+                } else {
+                    bulk_wait_read_all();
+                }
+            }
             __syncthreads();
             {
                 // row norms: lane 2v (v = 2i + s) forms the norm factor of value v
@@ -623,8 +651,69 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
             bulk_commit();
             if (nxt < n_items) issue_v(nxt, tok_next);  // v of this item is consumed
         }
+        prev = it;
+        it = nxt;
     }
-    if (tid == 0) bulk_wait_all();  // stores complete before the CTA releases its smem
+    if (tid == 0) {
+        bulk_wait_all();  // stores complete before the CTA releases its smem
+        if (p.ready && prev >= 0) publish_ready(p.ready + prev);
+    }
+}
+
+template <bool RAW16>
+__global__ void __launch_bounds__(kThreads, 1)
+kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    StaticClaims cl;
+    intra_items<RAW16>(maps, p, smem, cl);
+}
+
+// ---- fused intra + scan launch ---------------------------------------------
+// One CTA per SM, all resident at once (cooperative launch).  The CTAs take
+// work from one queue: positions [0, split) are intra items 0..split-1,
+// [split, split + n_walks) are scan walks, the rest intra items split.. .  The
+// CTAs that take a walk leave the intra work and run it; the others finish the
+// intra items, which each walk waits for (ready flags) chunk by chunk.  With
+// the split chosen so that the intra items stay ahead of the walks, the scan
+// runs alongside the second part of the intra work instead of after it.
+struct QueueClaims {
+    int* queue;
+    volatile int* slot;  // the claimed position, shared memory
+    int split, n_walks, n_items;
+    int last;  // the last claimed position
+    __device__ int item(int q) const {
+        return q < split ? q : (q < split + n_walks ? n_items : q - n_walks);
+    }
+    __device__ int first() {
+        if (threadIdx.x == 0) *slot = atomicAdd(queue, 1);
+        __syncthreads();
+        last = *slot;
+        __syncthreads();  // every thread has read it before the next claim
+        return item(last);
+    }
+    __device__ void claim() {
+        if (threadIdx.x == 0) *slot = atomicAdd(queue, 1);
+    }
+    __device__ int next(int) {
+        last = *slot;
+        return item(last);
+    }
+};
+
+template <bool RAW16>
+__global__ void __launch_bounds__(kThreads, 1)
+kda_fused(const __grid_constant__ IntraMaps maps, FwdParams p, int split, int n_walks) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    QueueClaims cl{p.queue, reinterpret_cast<volatile int*>(smem + kBar + 32), split, n_walks,
+                   p.n_chunks * p.H, -1};
+    intra_items<RAW16>(maps, p, smem, cl);
+    const int w = cl.last - split;
+    if (w < 0 || w >= n_walks || threadIdx.x >= scan::kScanThreads) return;
+    // walk w: (long sequence, head) pair w / 8, value rows 16 (w % 8) ..
+    const int pair = w >> 3;
+    const int sq = pair / p.H, h = pair % p.H;
+    const int n = p.long_list ? p.long_list[sq] : sq;
+    scan::scan_walk<2>(p, smem, n, h, w & 7);
 }
 
 // ---- host side -------------------------------------------------------------
@@ -660,18 +749,93 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elt,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_maps(IntraMaps* maps, const FwdParams& p) {
+    return make_map(&maps->q, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, p.H, p.T) &&
+           make_map(&maps->k, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, p.H, p.T) &&
+           make_map(&maps->v, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, p.H, p.T) &&
+           (p.raw_bf16 ? make_map(&maps->g, p.g_raw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, p.H, p.T)
+                       : make_map(&maps->g, p.g_raw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32, p.H, p.T));
+}
+
+// SMs kept on intra-chunk items once the walks have started, at least.
+constexpr int kFusedIntraSms = 32;
+// How many intra items one SM finishes while a walk advances by one chunk: a
+// walk step takes ~0.68 us and an item ~7.5 us on GB300 (ratio 0.09); 0.085 was
+// the fastest of 0.07 .. 0.125 on the 1 x 4096 and 1 x 16384, H = 12 prefills.
+constexpr double kItemsPerWalkStep = 0.085;
+
+// Per device: cooperative launch supported and one fused CTA fits on an SM.
+bool fused_device_ok() {
+    static int state[32] = {0};  // 0 unknown, 1 yes, 2 no
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev >= 32) return false;
+    if (!state[dev]) {
+        int coop = 0, per_sm = 0;
+        bool ok = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop;
+        ok = ok && cudaFuncSetAttribute(kda_fused<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kSmemBytes) == cudaSuccess;
+        ok = ok && cudaFuncSetAttribute(kda_fused<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kSmemBytes) == cudaSuccess;
+        ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_fused<false>, kThreads,
+                                                                 kSmemBytes) == cudaSuccess && per_sm >= 1;
+        ok = ok && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_fused<true>, kThreads,
+                                                                 kSmemBytes) == cudaSuccess && per_sm >= 1;
+        state[dev] = ok ? 1 : 2;
+    }
+    return state[dev] == 1;
+}
+
 }  // namespace
+
+bool fused_eligible(const FwdParams& p) {
+    if (!p.ready || !p.queue || p.n_chunks <= 0 || p.lower_bound < -5.0f) return false;
+    const int n_seq = p.long_list ? p.n_long : p.N;
+    if (n_seq <= 0) return false;
+    const int sms = num_sms();
+    if (scan_groups(n_seq, p.H, sms) != 1) return false;  // walks of 16 value rows
+    const long n_walks = (long)n_seq * p.H * (kD / 16);
+    return n_walks <= sms - kFusedIntraSms && fused_device_ok();
+}
+
+cudaError_t launch_fused(const FwdParams& p, cudaStream_t s) {
+    IntraMaps maps;
+    if (!make_maps(&maps, p)) return cudaErrorInvalidValue;
+    const int sms = num_sms();
+    const int n_seq = p.long_list ? p.n_long : p.N;
+    const int pairs = n_seq * p.H;
+    const int n_walks = pairs * (kD / 16);
+    const int n_items = p.n_chunks * p.H;
+    // Split: the walks start once the items done before them, plus what the
+    // remaining SMs finish meanwhile, keep each walk's next chunk ready: per
+    // chunk step the walks consume `pairs` items and the other SMs produce
+    // (sms - n_walks) * kItemsPerWalkStep.
+    const double steps = (double)p.n_chunks / n_seq;  // chunks per sequence, on average
+    const double deficit = pairs - (sms - n_walks) * kItemsPerWalkStep;
+    double split = pairs + (steps - 1.0) * (deficit > 0 ? deficit : 0.0);
+    if (split > n_items) split = n_items;
+    cudaError_t e = cudaMemsetAsync(p.queue, 0, sizeof(int), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p.ready, 0, (size_t)n_items * sizeof(int), s);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)sms);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int sp = (int)split;
+    if (p.raw_bf16) return cudaLaunchKernelEx(&cfg, kda_fused<true>, maps, p, sp, n_walks);
+    return cudaLaunchKernelEx(&cfg, kda_fused<false>, maps, p, sp, n_walks);
+}
 
 cudaError_t launch_intra(const FwdParams& p, cudaStream_t s) {
     if (p.n_chunks <= 0) return cudaSuccess;
     if (p.lower_bound < -5.0f) return launch_intra_exact(p, s);
     IntraMaps maps;
-    if (!make_map(&maps.q, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, p.H, p.T) ||
-        !make_map(&maps.k, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, p.H, p.T) ||
-        !make_map(&maps.v, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, p.H, p.T) ||
-        !(p.raw_bf16 ? make_map(&maps.g, p.g_raw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, p.H, p.T)
-                     : make_map(&maps.g, p.g_raw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32, p.H, p.T)))
-        return cudaErrorInvalidValue;
+    if (!make_maps(&maps, p)) return cudaErrorInvalidValue;
     static unsigned configured = 0;
     static int sms[32] = {0};
     int dev = 0;

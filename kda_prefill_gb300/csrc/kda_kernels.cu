@@ -1,16 +1,17 @@
-// Launch sequence of one KDA forward: the intra-chunk kernel (chunk-parallel),
-// the state scan (serial over each long sequence's chunks), then the
+// Launch sequence of one KDA forward: the intra-chunk kernel (chunk-parallel)
+// and the state scan (serial over each long sequence's chunks) -- or, when the
+// scan's walks leave enough SMs free, both in one fused launch -- then the
 // token-by-token kernel for the short sequences.
 #include "kda_internal.h"
 
 namespace kda {
 
 const char* kernel_name(int i) {
-    static const char* names[kNumKernels] = {"kda_intra", "kda_scan", "kda_decode"};
+    static const char* names[kNumKernels] = {"kda_intra", "kda_scan", "kda_fused", "kda_decode"};
     return (i >= 0 && i < kNumKernels) ? names[i] : nullptr;
 }
 
-static int num_sms() {
+int num_sms() {
     static int cached[32] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev >= 32) return 148;
@@ -24,23 +25,37 @@ static int num_sms() {
 
 unsigned launched_kernels(const FwdParams& p) {
     const int n_scan = p.long_list ? p.n_long : p.N;
-    return (p.n_chunks > 0 ? 1u : 0u) | (n_scan > 0 ? 2u : 0u) |
-           (p.n_short > 0 && p.short_list ? 4u : 0u);
+    const unsigned decode = (p.n_short > 0 && p.short_list) ? 8u : 0u;
+    if (fused_eligible(p)) return 4u | decode;
+    return (p.n_chunks > 0 ? 1u : 0u) | (n_scan > 0 ? 2u : 0u) | decode;
 }
 
 cudaError_t launch_forward(const FwdParams& p, cudaStream_t s, cudaEvent_t* marks) {
     cudaError_t e;
+    const bool fused = fused_eligible(p);
+    FwdParams q = p;  // the separate kernels neither publish nor wait for ready flags
+    q.ready = nullptr;
+    q.queue = nullptr;
     if (marks) cudaEventRecord(marks[0], s);
-    e = launch_intra(p, s);
-    if (e != cudaSuccess) return e;
+    if (!fused) {
+        e = launch_intra(q, s);
+        if (e != cudaSuccess) return e;
+    }
     if (marks) cudaEventRecord(marks[1], s);
-    const int n_scan = p.long_list ? p.n_long : p.N;
-    e = launch_scan(p, scan_groups(n_scan, p.H, num_sms()), s);
-    if (e != cudaSuccess) return e;
+    if (!fused) {
+        const int n_scan = q.long_list ? q.n_long : q.N;
+        e = launch_scan(q, scan_groups(n_scan, q.H, num_sms()), s);
+        if (e != cudaSuccess) return e;
+    }
     if (marks) cudaEventRecord(marks[2], s);
-    e = launch_decode(p, s);
-    if (e != cudaSuccess) return e;
+    if (fused) {
+        e = launch_fused(p, s);
+        if (e != cudaSuccess) return e;
+    }
     if (marks) cudaEventRecord(marks[3], s);
+    e = launch_decode(q, s);
+    if (e != cudaSuccess) return e;
+    if (marks) cudaEventRecord(marks[4], s);
     return cudaSuccess;
 }
 
