@@ -390,8 +390,11 @@ def load_traffic(kernel, workload):
         with open(path) as f:
             d = json.load(f)
         ent = d[kernel]
-        src = os.path.join(ROOT, ent["source"])
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        srcs = ent["source"] if isinstance(ent["source"], list) else [ent["source"]]
+        h = hashlib.sha256()
+        for src in srcs:
+            h.update(open(os.path.join(ROOT, src), "rb").read())
+        sha = h.hexdigest()[:16]
         if ent.get("source_sha") != sha or ent.get("workload") != workload:
             return None
         return ent["dram_bytes_per_launch"]

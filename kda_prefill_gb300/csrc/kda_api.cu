@@ -490,7 +490,8 @@ int run_forward(const void* q, const void* k, const void* v, const void* g_raw,
     (void)workspace_bytes;
 
     if (p.status) {
-        e = cudaMemsetAsync(p.status, 0, sizeof(int), stream);
+        // the status word and the fused launch's work counter, one memset
+        e = cudaMemsetAsync(p.status, 0, kda::kWsQueueOff + sizeof(int), stream);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (status)");
     }
     cudaEvent_t* marks = nullptr;
@@ -933,7 +934,8 @@ extern "C" int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v
     int32_t* lng = ctok + align4((size_t)bound);
     int32_t* sht = lng + align4((size_t)num_seqs);
 
-    cudaError_t e = cudaMemsetAsync(base, 0, sizeof(int), stream);  // status word
+    // the status word and the fused launch's work counter
+    cudaError_t e = cudaMemsetAsync(base, 0, kda::kWsQueueOff + sizeof(int), stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (status)");
     if (num_seqs > 0) {
         kda_noalloc_meta<<<1, 1024, 0, stream>>>(cu_seqlens, num_seqs, kChunk, mcu, off, cseq,

@@ -120,6 +120,7 @@ cudaError_t launch_decode(const FwdParams& p, cudaStream_t s);
 // Fused intra + scan launch (kda_intra_tc.cu), used instead of the two when
 // fused_eligible(p): the walks need few enough SMs, the device takes a
 // cooperative launch of one CTA per SM, and p.ready / p.queue are set.
+// The caller clears p.queue together with the status word before the launch.
 bool fused_eligible(const FwdParams& p);
 cudaError_t launch_fused(const FwdParams& p, cudaStream_t s);
 int num_sms();

@@ -39,6 +39,10 @@
 // the decay pass as fp16 pairs (a warp writes 128 contiguous bytes of a row);
 // w, u and A_qk are staged in shared memory in their workspace layout and
 // written by TMA bulk stores.
+//
+// The item loop is a device function shared by this kernel (static item
+// assignment) and the fused intra + scan launch at the end of the file, whose
+// CTAs take items and scan walks from one queue.
 
 #include <cuda.h>
 
@@ -813,8 +817,8 @@ cudaError_t launch_fused(const FwdParams& p, cudaStream_t s) {
     const double deficit = pairs - (sms - n_walks) * kItemsPerWalkStep;
     double split = pairs + (steps - 1.0) * (deficit > 0 ? deficit : 0.0);
     if (split > n_items) split = n_items;
-    cudaError_t e = cudaMemsetAsync(p.queue, 0, sizeof(int), s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(p.ready, 0, (size_t)n_items * sizeof(int), s);
+    // (the work counter is cleared with the status word by the caller)
+    cudaError_t e = cudaMemsetAsync(p.ready, 0, (size_t)n_items * sizeof(int), s);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)sms);
