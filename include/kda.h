@@ -251,6 +251,15 @@ KDA_API int kda_kernel_times(float* ms, int capacity, int* count, int* calls);
 KDA_API const char* kda_kernel_name(int i);
 
 /*
+ * Enables (default) or disables the fused intra-chunk + scan launch for the
+ * calls that follow, process-wide.  Disabled, every call runs the two kernels
+ * one after the other; results are bit-identical either way (same arithmetic),
+ * which makes this switch a check of the fused launch's hand-offs and a way to
+ * time the two schedules.  Returns KDA_OK.
+ */
+KDA_API int kda_set_fused_launch(int enable);
+
+/*
  * kda_chunk_fwd_noalloc — the paged forward for callers that cannot allocate
  * device memory.  The paper has no counterpart: this entry point exists for
  * integration only.

@@ -16,7 +16,7 @@ import torch
 __all__ = [
     "chunk_fwd", "chunk_fwd_dense", "workspace_size", "chunk_size", "plan_chunks",
     "release_cache", "cache_entries", "load_library", "KDAError", "STATE_DTYPES",
-    "set_kernel_timing", "kernel_times",
+    "set_kernel_timing", "kernel_times", "set_fused_launch",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -36,7 +36,7 @@ EXPORTED = (
     "kda_chunk_size", "kda_workspace_size", "kda_chunk_fwd", "kda_chunk_fwd_dense",
     "kda_plan_chunks", "kda_last_error", "kda_release_cache", "kda_cache_entries",
     "kda_set_kernel_timing", "kda_kernel_times", "kda_kernel_name", "kda_chunk_fwd_raw_bf16",
-    "kda_chunk_fwd_noalloc",
+    "kda_chunk_fwd_noalloc", "kda_set_fused_launch",
 )
 
 
@@ -95,6 +95,8 @@ def load_library(path: str = LIB_PATH):
     ]
     lib.kda_set_kernel_timing.restype = ctypes.c_int
     lib.kda_set_kernel_timing.argtypes = [ctypes.c_int]
+    lib.kda_set_fused_launch.restype = ctypes.c_int
+    lib.kda_set_fused_launch.argtypes = [ctypes.c_int]
     lib.kda_kernel_times.restype = ctypes.c_int
     lib.kda_kernel_times.argtypes = [_vp, ctypes.c_int, _vp, _vp]
     lib.kda_kernel_name.restype = ctypes.c_char_p
@@ -137,6 +139,12 @@ def cache_entries() -> int:
 def set_kernel_timing(enable: bool) -> None:
     lib = load_library()
     _check(lib.kda_set_kernel_timing(1 if enable else 0), lib)
+
+
+def set_fused_launch(enable: bool) -> None:
+    """Enables (default) or disables the fused intra + scan launch."""
+    lib = load_library()
+    _check(lib.kda_set_fused_launch(1 if enable else 0), lib)
 
 
 def kernel_times():

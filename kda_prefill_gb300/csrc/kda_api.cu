@@ -738,6 +738,11 @@ int kda_set_kernel_timing(int enable) {
     return KDA_OK;
 }
 
+int kda_set_fused_launch(int enable) {
+    kda::set_fused_enabled(enable != 0);
+    return KDA_OK;
+}
+
 int kda_kernel_times(float* ms, int capacity, int* count, int* calls) {
     std::lock_guard<std::mutex> lock(cache().mu);
     if (!ms || !count || !calls || capacity < kda::kNumKernels)

@@ -121,7 +121,9 @@ cudaError_t launch_decode(const FwdParams& p, cudaStream_t s);
 // fused_eligible(p): the walks need few enough SMs, the device takes a
 // cooperative launch of one CTA per SM, and p.ready / p.queue are set.
 // The caller clears p.queue together with the status word before the launch.
+// set_fused_enabled(false) makes every call use the separate kernels.
 bool fused_eligible(const FwdParams& p);
+void set_fused_enabled(bool on);
 cudaError_t launch_fused(const FwdParams& p, cudaStream_t s);
 int num_sms();
 int scan_groups(int N, int H, int num_sms);

@@ -46,6 +46,8 @@
 
 #include <cuda.h>
 
+#include <atomic>
+
 #include "kda_device.cuh"
 #include "kda_internal.h"
 #include "kda_scan_walk.cuh"
@@ -791,7 +793,11 @@ bool fused_device_ok() {
 
 }  // namespace
 
+static std::atomic<bool> g_fused_enabled{true};
+void set_fused_enabled(bool on) { g_fused_enabled.store(on); }
+
 bool fused_eligible(const FwdParams& p) {
+    if (!g_fused_enabled.load()) return false;
     if (!p.ready || !p.queue || p.n_chunks <= 0 || p.lower_bound < -5.0f) return false;
     const int n_seq = p.long_list ? p.n_long : p.N;
     if (n_seq <= 0) return false;
