@@ -106,8 +106,9 @@ KDA_API size_t kda_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_
  *                    s * state_stride0 + h * 128 * 128 + v * 128 + k.
  *   state_stride0    elements between slots, >= num_heads * 128 * 128; the
  *                    padding is never read or written.
- *   state_indices    device int32 [num_seqs], distinct slots in [0, num_slots)
- *                    (not checked on the device).
+ *   state_indices    device int32 [num_seqs], distinct slots in [0, num_slots).
+ *                    Distinctness is not checked; a slot outside the range is
+ *                    neither read nor written and reported by kda_check_status.
  *   has_initial_state device uint8 [num_seqs]: 0 starts the sequence from a
  *                    zero state and never reads its slot.
  *   out              device bf16 [total_tokens][num_heads][128], fully written;
@@ -249,6 +250,26 @@ KDA_API int kda_set_kernel_timing(int enable);
 KDA_API int kda_kernel_times(float* ms, int capacity, int* count, int* calls);
 /* Name of kernel i in launch order, or NULL. */
 KDA_API const char* kda_kernel_name(int i);
+
+/*
+ * Status word of the last call that used `workspace` (NULL: the built-in
+ * scratch of kda_chunk_fwd_noalloc), read after waiting for `stream`, the stream
+ * that call ran on.  *status is 0 when the call completed normally; otherwise an
+ * OR of KDA_STATUS_* bits.  Synchronises the stream, so it is not for use while
+ * the stream captures.  Returns KDA_OK, KDA_ERR_INVALID_ARG or KDA_ERR_CUDA.
+ *
+ * The pages keep synchronous state-index checks off the hot path (ROCm/aiter
+ * PR #5754, review findings); here the kernels compare each sequence's slot with
+ * num_slots (one comparison per CTA, no synchronisation) and skip the access of a
+ * slot outside the pool, and this call reports it afterwards.
+ */
+enum kda_status_bits {
+    KDA_STATUS_WAIT_TIMEOUT = 1, /* a bounded wait in a kernel gave up: results incomplete */
+    KDA_STATUS_SMEM_ALIGN = 2,   /* shared memory not 1 KB aligned: the intra kernel did nothing */
+    KDA_STATUS_BAD_SLOT = 4      /* a state index outside [0, num_slots): that sequence's
+                                    slot was neither read nor written */
+};
+KDA_API int kda_check_status(const void* workspace, kda_stream_t stream, int* status);
 
 /*
  * Enables (default) or disables the fused intra-chunk + scan launch for the

@@ -16,7 +16,8 @@ import torch
 __all__ = [
     "chunk_fwd", "chunk_fwd_dense", "workspace_size", "chunk_size", "plan_chunks",
     "release_cache", "cache_entries", "load_library", "KDAError", "STATE_DTYPES",
-    "set_kernel_timing", "kernel_times", "set_fused_launch",
+    "set_kernel_timing", "kernel_times", "set_fused_launch", "check_status",
+    "STATUS_WAIT_TIMEOUT", "STATUS_SMEM_ALIGN", "STATUS_BAD_SLOT",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -36,7 +37,7 @@ EXPORTED = (
     "kda_chunk_size", "kda_workspace_size", "kda_chunk_fwd", "kda_chunk_fwd_dense",
     "kda_plan_chunks", "kda_last_error", "kda_release_cache", "kda_cache_entries",
     "kda_set_kernel_timing", "kda_kernel_times", "kda_kernel_name", "kda_chunk_fwd_raw_bf16",
-    "kda_chunk_fwd_noalloc", "kda_set_fused_launch",
+    "kda_chunk_fwd_noalloc", "kda_set_fused_launch", "kda_check_status",
 )
 
 
@@ -97,6 +98,8 @@ def load_library(path: str = LIB_PATH):
     lib.kda_set_kernel_timing.argtypes = [ctypes.c_int]
     lib.kda_set_fused_launch.restype = ctypes.c_int
     lib.kda_set_fused_launch.argtypes = [ctypes.c_int]
+    lib.kda_check_status.restype = ctypes.c_int
+    lib.kda_check_status.argtypes = [_vp, _vp, _vp]
     lib.kda_kernel_times.restype = ctypes.c_int
     lib.kda_kernel_times.argtypes = [_vp, ctypes.c_int, _vp, _vp]
     lib.kda_kernel_name.restype = ctypes.c_char_p
@@ -139,6 +142,22 @@ def cache_entries() -> int:
 def set_kernel_timing(enable: bool) -> None:
     lib = load_library()
     _check(lib.kda_set_kernel_timing(1 if enable else 0), lib)
+
+
+STATUS_WAIT_TIMEOUT = 1
+STATUS_SMEM_ALIGN = 2
+STATUS_BAD_SLOT = 4
+
+
+def check_status(workspace: Optional[torch.Tensor] = None, stream=None) -> int:
+    """Status word of the last call that used `workspace` (None: the scratch of
+    the allocation-free entry point), after waiting for `stream` (default: the
+    current stream).  0 when it completed normally, else STATUS_* bits."""
+    lib = load_library()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    v = ctypes.c_int(0)
+    _check(lib.kda_check_status(_ptr(workspace), s.cuda_stream, ctypes.byref(v)), lib)
+    return int(v.value)
 
 
 def set_fused_launch(enable: bool) -> None:

@@ -412,6 +412,7 @@ struct StateArgs {
     const int32_t* in_idx;
     const int32_t* out_idx;
     const uint8_t* has_init;
+    int32_t num_slots;  // paged calls: slots are checked against it on the device; 0 = dense
 };
 
 int run_forward(const void* q, const void* k, const void* v, const void* g_raw,
@@ -486,6 +487,7 @@ int run_forward(const void* q, const void* k, const void* v, const void* g_raw,
     p.st_in_idx = st.in_idx;
     p.st_out_idx = st.out_idx;
     p.has_init = st.has_init;
+    p.num_slots = st.num_slots;
     p.st_dtype = state_dtype;
     (void)workspace_bytes;
 
@@ -560,6 +562,9 @@ int common_checks(const void* q, const void* k, const void* v, const void* g_raw
         return fail(KDA_ERR_UNSUPPORTED, "workspace is not 256-byte aligned");
     return KDA_OK;
 }
+
+// The allocation-free entry point's built-in scratch (defined further down).
+int noalloc_scratch(void** out);
 
 }  // namespace
 
@@ -647,7 +652,7 @@ int paged_forward(const void* q, const void* k, const void* v, const void* g_raw
             if (overlaps(rp, r)) return fail(KDA_ERR_INVALID_ARG, "state_cache overlaps %s", r.name);
     }
     StateArgs st{state_cache, state_cache, state_stride0, state_stride0,
-                 state_indices, state_indices, has_initial_state};
+                 state_indices, state_indices, has_initial_state, num_slots};
     return run_forward(q, k, v, g_raw, beta_raw, raw_bf16, cu_seqlens, cu_seqlens_host,
                        num_seqs, total_tokens, num_heads, st, state_dtype, out, lower_bound,
                        workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
@@ -715,7 +720,7 @@ int kda_chunk_fwd_dense(const void* q, const void* k, const void* v, const float
             overlaps(rf, rng("initial_state", initial_state, bytes)))
             return fail(KDA_ERR_INVALID_ARG, "final_state partially overlaps initial_state");
     }
-    StateArgs st{initial_state, final_state, plane, plane, nullptr, nullptr, has_initial_state};
+    StateArgs st{initial_state, final_state, plane, plane, nullptr, nullptr, has_initial_state, 0};
     return run_forward(q, k, v, g_raw, beta_raw, 0, cu_seqlens, cu_seqlens_host, num_seqs,
                        total_tokens, num_heads, st, state_dtype, out, lower_bound, workspace,
                        workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
@@ -735,6 +740,24 @@ int kda_cache_entries(void) {
 int kda_set_kernel_timing(int enable) {
     std::lock_guard<std::mutex> lock(cache().mu);
     timing().enabled = enable != 0;
+    return KDA_OK;
+}
+
+int kda_check_status(const void* workspace, kda_stream_t stream, int* status) {
+    if (!status) return fail(KDA_ERR_INVALID_ARG, "status is NULL");
+    const void* word = workspace;
+    if (!word) {  // the allocation-free entry point's built-in scratch
+        void* scratch = nullptr;
+        const int rc = noalloc_scratch(&scratch);
+        if (rc != KDA_OK) return rc;
+        word = scratch;
+    }
+    int v = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(&v, word, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "kda_check_status");
+    *status = v;
     return KDA_OK;
 }
 
@@ -980,6 +1003,7 @@ extern "C" int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v
     p.st_out_idx = state_indices;
     p.has_init = has_initial_state;
     p.st_dtype = state_dtype;
+    p.num_slots = num_slots;
     e = kda::launch_forward(p, stream, nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return KDA_OK;

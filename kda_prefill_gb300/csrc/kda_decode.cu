@@ -170,6 +170,13 @@ __global__ void __launch_bounds__(kDecThreadsAll, 3) kda_decode(FwdParams p, lon
                 init = p.has_init ? (p.has_init[n] != 0) : (p.st_in != nullptr);
                 in_slot = p.st_in_idx ? p.st_in_idx[n] : n;
                 out_slot = p.st_out_idx ? p.st_out_idx[n] : n;
+                if (p.num_slots > 0) {  // a slot outside the pool: no access, reported
+                    const bool bad_in = init && (in_slot < 0 || in_slot >= p.num_slots);
+                    const bool bad_out = out_slot < 0 || out_slot >= p.num_slots;
+                    if ((bad_in || bad_out) && p.status) atomicOr(p.status, 4);
+                    if (bad_in) init = 0;
+                    if (bad_out) out_slot = -1;  // no store
+                }
                 if (len > 0) braw = load_raw(p.beta_raw, p.raw_bf16, (size_t)tok0 * H + h);
             }
             bool stop = false;
@@ -270,7 +277,9 @@ __global__ void __launch_bounds__(kDecThreadsAll, 3) kda_decode(FwdParams p, lon
         const StageHeader* hd = reinterpret_cast<const StageHeader*>(stg + tile + kHdrOff);
         const int tok0 = hd->tok0, len = hd->len, h = hd->h, vb = hd->vb;
         const bool has_init = hd->has_init != 0;
-        const size_t out_base = (size_t)hd->out_slot * p.st_out_stride + (size_t)h * D * D;
+        const bool store_ok = hd->out_slot >= 0;
+        const size_t out_base =
+            store_ok ? (size_t)hd->out_slot * p.st_out_stride + (size_t)h * D * D : 0;
         float braw = hd->beta_raw;
 
         float S[8][8];  // rows vb + 16 warp + 2j + hw, keys k0..k0+7
@@ -374,10 +383,12 @@ __global__ void __launch_bounds__(kDecThreadsAll, 3) kda_decode(FwdParams p, lon
             csync();  // the next token rewrites the shared vectors
         }
 
+        if (store_ok) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int vr = vb + 16 * warp + 2 * j + hw;
-            store8(p.st_out, p.st_dtype, out_base + (size_t)vr * D + k0, S[j]);
+            for (int j = 0; j < 8; ++j) {
+                const int vr = vb + 16 * warp + 2 * j + hw;
+                store8(p.st_out, p.st_dtype, out_base + (size_t)vr * D + k0, S[j]);
+            }
         }
     }
 }

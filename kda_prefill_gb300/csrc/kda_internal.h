@@ -84,6 +84,9 @@ struct FwdParams {
     const int32_t* st_out_idx;
     const uint8_t* has_init;  // nullptr: every sequence has one iff st_in != nullptr
     int st_dtype;             // 0 fp32, 1 bf16, 2 fp16
+    // pool slots of a paged call: a slot outside [0, num_slots) is neither read
+    // nor written, and the status word gets bit 2 (value 4); 0 = not checked
+    int num_slots;
 };
 
 // Element i of a raw gate / beta array (fp32, or bf16 when raw_bf16 is set).

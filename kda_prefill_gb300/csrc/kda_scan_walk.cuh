@@ -261,11 +261,19 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
         return *abort_flag;
     };
 
-    const bool has_init = p.has_init ? (p.has_init[n] != 0) : (p.st_in != nullptr);
+    bool has_init = p.has_init ? (p.has_init[n] != 0) : (p.st_in != nullptr);
     const int64_t in_slot = p.st_in_idx ? p.st_in_idx[n] : n;
     const int64_t out_slot = p.st_out_idx ? p.st_out_idx[n] : n;
-    const size_t in_base = (size_t)in_slot * p.st_in_stride + (size_t)h * D * D;
-    const size_t out_base = (size_t)out_slot * p.st_out_stride + (size_t)h * D * D;
+    bool store_ok = true;
+    if (p.num_slots > 0) {  // a slot outside the pool: no access, reported
+        const bool bad_in = has_init && (in_slot < 0 || in_slot >= p.num_slots);
+        const bool bad_out = out_slot < 0 || out_slot >= p.num_slots;
+        if ((bad_in || bad_out) && wr == 0 && lane == 0 && p.status) atomicOr(p.status, 4);
+        if (bad_in) has_init = false;
+        if (bad_out) store_ok = false;
+    }
+    const size_t in_base = has_init ? (size_t)in_slot * p.st_in_stride + (size_t)h * D * D : 0;
+    const size_t out_base = store_ok ? (size_t)out_slot * p.st_out_stride + (size_t)h * D * D : 0;
 
     float Sm[2][NT][4];  // [mt][nt][e]: k = 32wr+16mt+g+8(e>>1), v = 8nt+2tq+(e&1)
 #pragma unroll
@@ -413,7 +421,7 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
             break;
         }
     }
-    if (failed) return;
+    if (failed || !store_ok) return;
 
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)

@@ -7,7 +7,7 @@ import torch
 
 import kda_prefill_gb300 as kda
 from kda_prefill_gb300 import workloads as wl
-from tests.gpu_helpers import DevRun, TOL, compare, unselected_untouched, rel_l2
+from tests.gpu_helpers import DevRun, TOL, compare, oracle_paged, unselected_untouched, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -236,3 +236,50 @@ def test_serving_workload_sampled_heads(name, heads):
     print(f"{name}: out rel-L2 {eo:.3e}, state rel-L2 {es:.3e}")
     assert unselected_untouched(r, before)
     assert torch.isfinite(r.out.float()).all()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("fused", [True, False])
+def test_bad_state_index_is_skipped_and_reported(fused):
+    """A slot outside [0, num_slots) is neither read nor written and shows in the
+    status word; the other sequences are unaffected (the walks check the long
+    sequences' slots, the token-by-token kernel the short one's)."""
+    import copy
+    lengths = [130, 70, 3, 90]
+    w = wl.make_workload("bad_slot", lengths, 2, num_slots=6, state_indices=[1, 6, -3, 4],
+                         has_initial_state=[1, 1, 1, 0], seed=51)
+    # the oracle on the same inputs with harmless slots for the two bad sequences
+    ref = copy.copy(w)
+    ref.state_indices = torch.tensor([1, 2, 3, 4], dtype=torch.int32)
+    ref.has_initial_state = torch.tensor([True, False, False, False])
+    o_ref, f_ref = oracle_paged(ref)
+    r = DevRun(w)
+    before = r.storage.cpu().clone()
+    ws = torch.empty(kda.workspace_size(w.total_tokens, w.num_seqs, w.num_heads),
+                     dtype=torch.uint8, device="cuda")
+    kda.set_fused_launch(fused)
+    try:
+        r.run(workspace=ws)
+        status = kda.check_status(ws)
+    finally:
+        kda.set_fused_launch(True)
+    assert status == kda.STATUS_BAD_SLOT
+    after = r.storage.cpu()
+    for slot in (0, 2, 3, 5):  # no valid sequence writes them, the bad ones must not
+        assert torch.equal(after[slot].view(torch.int32), before[slot].view(torch.int32))
+    cu = w.cu_seqlens.tolist()
+    for n, slot in ((0, 1), (3, 4)):
+        o_gpu = r.out[0, cu[n]:cu[n + 1]].double().cpu().numpy()
+        assert rel_l2(o_gpu, o_ref[cu[n]:cu[n + 1]]) <= TOL[torch.float32]
+        f_gpu = r.pool[slot].double().cpu().numpy()
+        assert rel_l2(f_gpu, f_ref[n]) <= TOL[torch.float32]
+
+
+@pytest.mark.gpu
+def test_status_is_clear_after_a_normal_call():
+    w = wl.tiny_varlen()
+    r = DevRun(w)
+    ws = torch.empty(kda.workspace_size(w.total_tokens, w.num_seqs, w.num_heads),
+                     dtype=torch.uint8, device="cuda")
+    r.run(workspace=ws)
+    assert kda.check_status(ws) == 0
