@@ -61,6 +61,8 @@ def parse():
     ap.add_argument("--workload", default="prefill_16k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--meta-miss", action="store_true",
+                    help="also time calls whose bounds are new to the metadata cache")
     ap.add_argument("--clock-seconds", type=float, default=1.5,
                     help="minimum span of the nvidia-smi clock sampling")
     return ap.parse_args()
@@ -265,6 +267,41 @@ def run_ours(args, rank, world):
     kda.set_kernel_timing(False)
     kavg = {n: t / max(kcalls, 1) for n, t in ktimes.items()}
 
+    # metadata-cache misses: every step's bounds are new (a permutation of the
+    # same sequence lengths over the same packed tensors), so each call builds
+    # its chunk table on the host and uploads it before the kernels
+    meta_miss = None
+    if args.meta_miss:
+        gen = torch.Generator().manual_seed(1234)
+        lens = torch.tensor(w.lengths, dtype=torch.int64)
+        sets = []
+        for _ in range(args.warmup + args.steps):
+            cu_h = torch.zeros(N + 1, dtype=torch.int32)
+            cu_h[1:] = torch.cumsum(lens[torch.randperm(N, generator=gen)], 0).to(torch.int32)
+            sets.append((cu_h, cu_h.to(dev)))
+
+        def step_miss(i):
+            cu_h, cu_d = sets[i]
+            kda.chunk_fwd(q, k, v, g, b, cu_d, state_cache=pool, state_indices=idx,
+                          has_initial_state=hs, out=out, lower_bound=w.lower_bound,
+                          cu_seqlens_cpu=cu_h, workspace=ws)
+
+        for i in range(args.warmup):
+            step_miss(i)
+        torch.cuda.synchronize(dev)
+        barrier()
+        m0 = torch.cuda.Event(enable_timing=True)
+        m1 = torch.cuda.Event(enable_timing=True)
+        m0.record(stream)
+        for i in range(args.steps):
+            step_miss(args.warmup + i)
+        m1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        miss_ms = max_over_ranks(m0.elapsed_time(m1)) / args.steps
+        meta_miss = {"us_per_call": miss_ms * 1e3, "hit_us_per_call": ms_step * 1e3,
+                     "bound_sets": args.warmup + args.steps}
+
     # end to end through the public API with host buffers: every step uploads
     # its inputs from pinned host memory and reads its output back.  Uploads,
     # forwards and read-backs run on three streams over two device buffer sets,
@@ -374,6 +411,7 @@ def run_ours(args, rank, world):
         "kernels_us": {n: t * 1e3 for n, t in kavg.items()},
         "clocks": clocks,
         "e2e": e2e,
+        **({"metadata_miss": meta_miss} if meta_miss else {}),
         "gpu_launches": n_launch_per_step * args.steps,
     }
     if world == 1 and not args.no_cpu_baseline:
