@@ -777,7 +777,9 @@ int kda_kernel_times(float* ms, int capacity, int* count, int* calls) {
     for (size_t j = 0; j < t.calls.size(); ++j) {
         const auto& c = t.calls[j];
         const unsigned ran = t.launched[j];
-        cudaError_t e = cudaEventSynchronize(c.back());
+        cudaError_t e = cudaSuccess;
+        for (cudaEvent_t ev : c)  // the marks may sit on several streams
+            if (e == cudaSuccess) e = cudaEventSynchronize(ev);
         if (e != cudaSuccess) rc = cuda_fail(e, "cudaEventSynchronize");
         for (int i = 0; i < kda::kNumKernels && rc == KDA_OK; ++i) {
             if (!(ran & (1u << i))) continue;  // not launched: no time

@@ -20,8 +20,19 @@ def _workspace(w):
 
 
 @pytest.mark.gpu
-def test_captured_call_replays_like_eager_calls():
+@pytest.mark.parametrize("fused", [True, False])
+def test_captured_call_replays_like_eager_calls(fused):
+    """fused=False: the intra-chunk kernel, the scan and the token-by-token
+    kernel as separate launches."""
     assert torch.cuda.is_available(), "GPU test"
+    kda.set_fused_launch(fused)
+    try:
+        _captured_call_replays_like_eager_calls()
+    finally:
+        kda.set_fused_launch(True)
+
+
+def _captured_call_replays_like_eager_calls():
     # long, short (token by token) and empty sequences in one batch
     w = wl.make_workload("graph", [300, 1, 130, 0, 5], 2, num_slots=8, seed=31,
                          has_initial_state=[1, 1, 0, 1, 0], stride_pad=64)
