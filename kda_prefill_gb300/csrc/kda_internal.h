@@ -124,7 +124,10 @@ cudaError_t launch_decode(const FwdParams& p, cudaStream_t s);
 // fused_eligible(p): the walks need few enough SMs, the device takes a
 // cooperative launch of one CTA per SM, and p.ready / p.queue are set.
 // The caller clears p.queue together with the status word before the launch.
-// set_fused_enabled(false) makes every call use the separate kernels.
+// set_fused_enabled(false) makes every call use the separate kernels.  When the
+// device refuses the cooperative launch, launch_fused returns
+// cudaErrorCooperativeLaunchTooLarge having enqueued nothing but the flag reset,
+// and the device is not offered the fused launch again.
 bool fused_eligible(const FwdParams& p);
 void set_fused_enabled(bool on);
 cudaError_t launch_fused(const FwdParams& p, cudaStream_t s);

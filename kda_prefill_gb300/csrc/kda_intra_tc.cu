@@ -771,8 +771,10 @@ constexpr int kFusedIntraSms = 32;
 constexpr double kItemsPerWalkStep = 0.085;
 
 // Per device: cooperative launch supported and one fused CTA fits on an SM.
+int g_fused_state[32] = {0};  // per device: 0 unknown, 1 usable, 2 not
+
 bool fused_device_ok() {
-    static int state[32] = {0};  // 0 unknown, 1 yes, 2 no
+    int* state = g_fused_state;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev >= 32) return false;
     if (!state[dev]) {
@@ -837,8 +839,13 @@ cudaError_t launch_fused(const FwdParams& p, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const int sp = (int)split;
-    if (p.raw_bf16) return cudaLaunchKernelEx(&cfg, kda_fused<true>, maps, p, sp, n_walks);
-    return cudaLaunchKernelEx(&cfg, kda_fused<false>, maps, p, sp, n_walks);
+    e = p.raw_bf16 ? cudaLaunchKernelEx(&cfg, kda_fused<true>, maps, p, sp, n_walks)
+                   : cudaLaunchKernelEx(&cfg, kda_fused<false>, maps, p, sp, n_walks);
+    if (e == cudaErrorCooperativeLaunchTooLarge) {  // fewer SMs than expected are ours
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess && dev < 32) g_fused_state[dev] = 2;
+    }
+    return e;
 }
 
 cudaError_t launch_intra(const FwdParams& p, cudaStream_t s) {

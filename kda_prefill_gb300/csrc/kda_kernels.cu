@@ -30,6 +30,8 @@ unsigned launched_kernels(const FwdParams& p) {
     return (p.n_chunks > 0 ? 1u : 0u) | (n_scan > 0 ? 2u : 0u) | decode;
 }
 
+static int n_scan_of(const FwdParams& p) { return p.long_list ? p.n_long : p.N; }
+
 cudaError_t launch_forward(const FwdParams& p, cudaStream_t s, cudaEvent_t* marks) {
     cudaError_t e;
     const bool fused = fused_eligible(p);
@@ -50,6 +52,13 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t s, cudaEvent_t* mark
     if (marks) cudaEventRecord(marks[2], s);
     if (fused) {
         e = launch_fused(p, s);
+        if (e == cudaErrorCooperativeLaunchTooLarge) {
+            // the device refused the cooperative launch (and is marked so for
+            // later calls): run the two kernels instead
+            (void)cudaGetLastError();
+            e = launch_intra(q, s);
+            if (e == cudaSuccess) e = launch_scan(q, scan_groups(n_scan_of(q), q.H, num_sms()), s);
+        }
         if (e != cudaSuccess) return e;
     }
     if (marks) cudaEventRecord(marks[3], s);
