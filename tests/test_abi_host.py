@@ -193,3 +193,18 @@ def test_dense_rejects_overlapping_final_state(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(ImportError):
         kda.load_library(str(tmp_path / "missing.so"))
+
+
+def test_status_and_switch_entry_points(lib):
+    # kda_check_status rejects a missing output before touching CUDA
+    rc = lib.kda_check_status(None, None, None)
+    assert rc == kda.KDA_ERR_INVALID_ARG
+    assert "status" in lib.kda_last_error().decode()
+    # the fused-launch switch is host state only
+    assert lib.kda_set_fused_launch(0) == kda.KDA_OK
+    assert lib.kda_set_fused_launch(1) == kda.KDA_OK
+    # four kernels in launch order, the fused launch between the scan and the
+    # token-by-token kernel
+    names = [lib.kda_kernel_name(i).decode() for i in range(4)]
+    assert names == ["kda_intra", "kda_scan", "kda_fused", "kda_decode"]
+    assert lib.kda_kernel_name(4) is None
