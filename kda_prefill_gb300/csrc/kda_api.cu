@@ -89,6 +89,7 @@ int check_host_bounds(const int32_t* cu, int32_t N, int64_t T) {
 struct MetaLayout {
     int64_t n_chunks = 0;
     int32_t n_long = 0, n_short = 0;
+    int32_t max_long_chunks = 0;  // chunks of the longest sequence the chunked kernels take
     size_t off_cu = 0, off_seq_off = 0, off_chunk_seq = 0, off_chunk_tok = 0;  // int32 units
     size_t off_long = 0, off_short = 0;
     size_t words = 0;
@@ -103,6 +104,7 @@ MetaLayout meta_layout(const int32_t* cu, int32_t N) {
         const int64_t len = (int64_t)cu[n + 1] - cu[n];
         L.n_chunks += routed_chunks(len);
         if (is_short(len)) ++L.n_short; else ++L.n_long;
+        L.max_long_chunks = std::max<int32_t>(L.max_long_chunks, (int32_t)routed_chunks(len));
     }
     size_t o = 0;
     L.off_cu = o;        o = align4(o + (size_t)N + 1);
@@ -480,6 +482,8 @@ int run_forward(const void* q, const void* k, const void* v, const void* g_raw,
     p.status = ws ? reinterpret_cast<int*>(ws) : nullptr;
     p.queue = ws ? reinterpret_cast<int*>(ws + kda::kWsQueueOff) : nullptr;
     p.ready = ws ? reinterpret_cast<int*>(ws + kda::flags_offset(max_chunks(T, N), H)) : nullptr;
+    p.seg = ws ? reinterpret_cast<float*>(ws + kda::seg_offset(max_chunks(T, N), H)) : nullptr;
+    p.max_long_chunks = m->layout.max_long_chunks;
     p.st_in = st.in;
     p.st_out = st.out;
     p.st_in_stride = st.in_stride;
@@ -948,11 +952,12 @@ extern "C" int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v
                         "state_cache and its slot stride must be 16-byte aligned");
     }
     int64_t n_chunks = 0;
-    int32_t n_long = 0;
+    int32_t n_long = 0, max_long = 0;
     for (int32_t n = 0; n < num_seqs; ++n) {
         const int64_t len = (int64_t)cu_seqlens_host[n + 1] - cu_seqlens_host[n];
         n_chunks += routed_chunks(len);
         n_long += is_short(len) ? 0 : 1;
+        max_long = std::max<int32_t>(max_long, (int32_t)routed_chunks(len));
     }
 
     uint8_t* base = static_cast<uint8_t*>(scratch);
@@ -997,6 +1002,8 @@ extern "C" int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v
     p.status = reinterpret_cast<int*>(base);
     p.queue = reinterpret_cast<int*>(base + kda::kWsQueueOff);
     p.ready = reinterpret_cast<int*>(base + kda::flags_offset(bound, num_heads));
+    p.seg = reinterpret_cast<float*>(base + kda::seg_offset(bound, num_heads));
+    p.max_long_chunks = max_long;
     p.st_in = state_cache;
     p.st_out = state_cache;
     p.st_in_stride = state_stride0;

@@ -87,6 +87,11 @@ struct FwdParams {
     // pool slots of a paged call: a slot outside [0, num_slots) is neither read
     // nor written, and the status word gets bit 2 (value 4); 0 = not checked
     int num_slots;
+
+    // segmented scan (few long sequences): chunks of the longest long sequence,
+    // and the workspace area of the segments' fp32 state planes (nullptr: none)
+    int max_long_chunks;
+    float* seg;
 };
 
 // Element i of a raw gate / beta array (fp32, or bf16 when raw_bf16 is set).
@@ -98,8 +103,15 @@ __device__ __forceinline__ float load_raw(const void* p, int raw_bf16, size_t i)
 inline size_t flags_offset(int64_t max_chunks, int H) {
     return (size_t)kWsHeader + (size_t)max_chunks * (size_t)H * (size_t)kWsBytes;
 }
-inline size_t workspace_bytes(int64_t max_chunks, int H) {
+// The segmented scan's fp32 [128][128] state planes (at most kSegPlanes: three
+// per segment boundary, with (pairs) x (segments - 1) <= 152 / 16) follow the flags.
+constexpr int kSegPlaneFloats = 128 * 128;
+constexpr int kSegPlanes = 32;
+inline size_t seg_offset(int64_t max_chunks, int H) {
     return flags_offset(max_chunks, H) + (((size_t)max_chunks * (size_t)H * 4 + 255) & ~size_t(255));
+}
+inline size_t workspace_bytes(int64_t max_chunks, int H) {
+    return seg_offset(max_chunks, H) + (size_t)kSegPlanes * kSegPlaneFloats * 4;
 }
 
 // Number of kernels one forward launches, and their names (launch order).
@@ -133,5 +145,8 @@ void set_fused_enabled(bool on);
 cudaError_t launch_fused(const FwdParams& p, cudaStream_t s);
 int num_sms();
 int scan_groups(int N, int H, int num_sms);
+// Segments per long sequence when the scan runs segmented (few (sequence, head)
+// pairs, so that the segments' walks fill the GPU), else 0; *L = chunks per segment.
+int scan_segments(const FwdParams& p, int num_sms, int* L);
 
 }  // namespace kda

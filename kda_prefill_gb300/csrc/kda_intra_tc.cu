@@ -805,6 +805,8 @@ bool fused_eligible(const FwdParams& p) {
     if (n_seq <= 0) return false;
     const int sms = num_sms();
     if (scan_groups(n_seq, p.H, sms) != 1) return false;  // walks of 16 value rows
+    int seg_len = 0;
+    if (scan_segments(p, sms, &seg_len) > 0) return false;  // the segmented scan does better
     const long n_walks = (long)n_seq * p.H * (kD / 16);
     return n_walks <= sms - kFusedIntraSms && fused_device_ok();
 }

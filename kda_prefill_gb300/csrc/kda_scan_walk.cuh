@@ -92,8 +92,25 @@ __device__ __forceinline__ void store_state(void* base, int dtype, size_t off, f
 // shared memory at `smem` (1 KB aligned, ScanSmem<NT>::kTotal bytes).  With
 // p.ready set, each chunk's operands are fetched only once their block is
 // marked written (the fused launch, where the intra-chunk work runs alongside).
+// What a walk covers, where its state starts and where it ends.  The default
+// walks the whole sequence from its pool (or zero) state, writes the outputs
+// and writes the final state back to the pool.  The segmented scan walks a
+// range of chunks from a zero state, from identity rows with u = 0 (the range's
+// transition), or from a given fp32 state.
+struct WalkRange {
+    int first = 0;                // first chunk of the sequence
+    int count = -1;               // chunks to walk; -1: to the end
+    int init = 0;                 // 0: pool per has_initial_state, 1: zero, 2: identity rows, 3: init_buf
+    const float* init_buf = nullptr;  // init 3: [128][128] fp32, rows = value rows
+    bool zero_u = false;          // u taken as 0
+    bool outputs = true;          // write o
+    bool final_state = true;      // write the final state
+    float* final_buf = nullptr;   // ... into this [128][128] fp32 plane instead of the pool
+};
+
 template <int NT>
-__device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int n, int h, int z) {
+__device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int n, int h, int z,
+                                          const WalkRange& R = WalkRange()) {
     using L = ScanSmem<NT>;
     constexpr int VS = L::VS;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);  // [kStages]
@@ -108,10 +125,11 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
     const int g = lane >> 2, tq = lane & 3;
     const int mi = lane >> 3, rr = lane & 7;  // ldmatrix / stmatrix addressing
 
-    const int tok0 = p.cu[n];
-    const int len = p.cu[n + 1] - tok0;
-    const int c0 = p.seq_off[n];
-    const int nch = p.seq_off[n + 1] - c0;
+    const int tok0 = p.cu[n] + R.first * C;  // token of the walk's first chunk
+    const int len = p.cu[n + 1] - tok0;         // tokens from there to the sequence end
+    const int c0 = p.seq_off[n] + R.first;
+    const int left = p.seq_off[n + 1] - c0;
+    const int nch = R.count < 0 || R.count > left ? left : R.count;
 
     const uint32_t sm_base = smem_u32(smem);
     auto stage_base = [&](int s) { return sm_base + s * L::kStage; };
@@ -233,7 +251,7 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const int i = 16 * wr + g + 8 * hh;
-                if (lc * C + i < len) {
+                if (R.outputs && lc * C + i < len) {
                     const size_t t = (size_t)(tok0 + lc * C + i);
                     __nv_bfloat16* orow = p.out + (t * p.H + h) * D + v0;
 #pragma unroll
@@ -261,13 +279,13 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
         return *abort_flag;
     };
 
-    bool has_init = p.has_init ? (p.has_init[n] != 0) : (p.st_in != nullptr);
+    bool has_init = R.init == 0 && (p.has_init ? (p.has_init[n] != 0) : (p.st_in != nullptr));
     const int64_t in_slot = p.st_in_idx ? p.st_in_idx[n] : n;
     const int64_t out_slot = p.st_out_idx ? p.st_out_idx[n] : n;
-    bool store_ok = true;
+    bool store_ok = R.final_state;
     if (p.num_slots > 0) {  // a slot outside the pool: no access, reported
         const bool bad_in = has_init && (in_slot < 0 || in_slot >= p.num_slots);
-        const bool bad_out = out_slot < 0 || out_slot >= p.num_slots;
+        const bool bad_out = R.final_state && !R.final_buf && (out_slot < 0 || out_slot >= p.num_slots);
         if ((bad_in || bad_out) && wr == 0 && lane == 0 && p.status) atomicOr(p.status, 4);
         if (bad_in) has_init = false;
         if (bad_out) store_ok = false;
@@ -285,7 +303,10 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
                 const int kk = 32 * wr + 16 * mt + g + 8 * (e >> 1);
                 const int vv = v0 + 8 * nt + 2 * tq + (e & 1);
                 Sm[mt][nt][e] =
-                    has_init ? load_state(p.st_in, p.st_dtype, in_base + (size_t)vv * D + kk) : 0.f;
+                    has_init     ? load_state(p.st_in, p.st_dtype, in_base + (size_t)vv * D + kk)
+                    : R.init == 2 ? (kk == vv ? 1.f : 0.f)
+                    : R.init == 3 ? R.init_buf[(size_t)vv * D + kk]
+                                  : 0.f;
             }
 
     // S (fp16) into ring slot b: S^T fragments stored transposed as S[v][k].
@@ -354,7 +375,8 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
                 asm volatile("ld.shared.b32 %0, [%1];"
                              : "=r"(uv)
                              : "r"(tu + (vv >> 4) * kWsUSliceBytes + (i * 16 + (vv & 15)) * 2));
-                const float2 u2 = __half22float2(*reinterpret_cast<__half2*>(&uv));
+                const float2 u2 = R.zero_u ? make_float2(0.f, 0.f)
+                                           : __half22float2(*reinterpret_cast<__half2*>(&uv));
                 uf[nt][hh] = pack_half2(u2.x - accU[nt][2 * hh] - accU2[nt][2 * hh],
                                         u2.y - accU[nt][2 * hh + 1] - accU2[nt][2 * hh + 1]);
             }
@@ -431,7 +453,10 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
             for (int e = 0; e < 4; ++e) {
                 const int kk = 32 * wr + 16 * mt + g + 8 * (e >> 1);
                 const int vv = v0 + 8 * nt + 2 * tq + (e & 1);
-                store_state(p.st_out, p.st_dtype, out_base + (size_t)vv * D + kk, Sm[mt][nt][e]);
+                if (R.final_buf)
+                    R.final_buf[(size_t)vv * D + kk] = Sm[mt][nt][e];
+                else
+                    store_state(p.st_out, p.st_dtype, out_base + (size_t)vv * D + kk, Sm[mt][nt][e]);
             }
 }
 

@@ -179,6 +179,15 @@ def prefill_16k_raw_bf16() -> Workload:
     return w
 
 
+def prefill_16k_h2() -> Workload:
+    """1 x 16384 tokens with 2 heads (a few-head shard of the long prefill),
+    contiguous fp32 pool of 8 slots, no initial state."""
+    w = make_workload("prefill_1x16384_h2", [16384], 2, num_slots=8,
+                      state_indices=[0], has_initial_state=[0], seed=6)
+    poison_unread_slots(w)
+    return w
+
+
 def _varlen_lengths(g: torch.Generator, n: int = 128, max_len: int = 2048,
                     p_empty: float = 0.05):
     empty = torch.rand(n, generator=g) < p_empty
@@ -211,6 +220,7 @@ WORKLOADS = {
     "prefill_4k": prefill_4k,
     "prefill_16k": prefill_16k,
     "prefill_16k_raw_bf16": prefill_16k_raw_bf16,
+    "prefill_16k_h2": prefill_16k_h2,
     "varlen_batch": varlen_batch,
     "mixed_bf16_pool": mixed_bf16_pool,
 }

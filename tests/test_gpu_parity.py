@@ -283,3 +283,32 @@ def test_status_is_clear_after_a_normal_call():
                      dtype=torch.uint8, device="cuda")
     r.run(workspace=ws)
     assert kda.check_status(ws) == 0
+
+
+SEGMENTED_CASES = [
+    # at most 4 (sequence, head) pairs with long sequences: the scan runs
+    # segmented (pass A, combine, pass B)
+    ([3000], 1, torch.float32, 0, [1]),                 # one pair, 10 segments of 5 chunks
+    ([1000, 700, 5], 2, torch.float16, 32, [1, 0, 1]),  # 4 pairs, 3 and 2 segments, one short
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("lengths,H,dt,pad,flags", SEGMENTED_CASES)
+def test_segmented_scan(lengths, H, dt, pad, flags):
+    w = wl.make_workload("segmented", lengths, H, num_slots=len(lengths) + 3, pool_dtype=dt,
+                         stride_pad=pad, has_initial_state=flags, seed=sum(lengths) + H)
+    wl.poison_unread_slots(w)
+    r = DevRun(w)
+    before = r.storage.cpu().clone()
+    kda.set_kernel_timing(True)
+    kda.kernel_times()
+    try:
+        r.run()
+        torch.cuda.synchronize()
+        times, _ = kda.kernel_times()
+    finally:
+        kda.set_kernel_timing(False)
+    assert times["kda_fused"] == 0.0 and times["kda_scan"] > 0.0, times
+    compare(r, tol=TOL[dt])
+    assert unselected_untouched(r, before)
