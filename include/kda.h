@@ -125,9 +125,11 @@ KDA_API size_t kda_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_
  * Sequences of more than 8 tokens run through the chunked kernels (intra-chunk
  * tiles, then the state scan; when the scan needs few SMs, both in one
  * cooperative launch where the scan follows the intra-chunk work chunk by
- * chunk); sequences of at most 8 tokens (decode steps, empty sequences) run
- * token by token in another kernel with the state in fp32 registers.  Both
- * compute the same recurrence; only rounding differs.
+ * chunk; for at most 4 (sequence, head) pairs of long sequences, the scan in
+ * segments walked in parallel and chained through the segments' transitions);
+ * sequences of at most 8 tokens (decode steps, empty sequences) run token by
+ * token in another kernel with the state in fp32 registers.  All compute the
+ * same recurrence; only rounding differs.
  *
  * CUDA graph capture: a call on a capturing stream is captured when
  * cu_seqlens_host is given and an earlier call, finished before the capture
