@@ -310,7 +310,8 @@ KDA_API int kda_set_fused_launch(int enable);
  * call's contents: calls that overlap on the GPU race and give wrong results,
  * so order them (one stream, or events).  It calls no cudaMalloc, cudaFree or
  * other allocating routine.  Results equal kda_chunk_fwd's: same kernels, same
- * chunk table.
+ * chunk table.  Its arguments pass kda_chunk_fwd's host checks (activations,
+ * bounds, pool, overlaps) before any CUDA call, with the same error codes.
  */
 #define KDA_NOALLOC_SCRATCH_BYTES (64ull << 20)
 KDA_API int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v,

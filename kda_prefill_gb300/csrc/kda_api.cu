@@ -516,11 +516,12 @@ int run_forward(const void* q, const void* k, const void* v, const void* g_raw,
     return KDA_OK;
 }
 
-int common_checks(const void* q, const void* k, const void* v, const void* g_raw,
-                  const void* beta_raw, int raw_bf16, const int32_t* cu_dev,
-                  const int32_t* cu_host, int32_t N, int64_t T, int32_t H, void* out,
-                  float lower_bound, int state_dtype, void* workspace,
-                  size_t workspace_bytes) {
+// Checks of the activations, bounds, dtype and lower bound (everything but the
+// state and the workspace).
+int input_checks(const void* q, const void* k, const void* v, const void* g_raw,
+                 const void* beta_raw, int raw_bf16, const int32_t* cu_dev,
+                 const int32_t* cu_host, int32_t N, int64_t T, int32_t H, void* out,
+                 float lower_bound, int state_dtype) {
     if (N < 0) return fail(KDA_ERR_INVALID_ARG, "num_seqs = %d < 0", N);
     if (T < 0) return fail(KDA_ERR_INVALID_ARG, "total_tokens = %lld < 0", (long long)T);
     if (T > INT32_MAX - kChunk)
@@ -558,6 +559,17 @@ int common_checks(const void* q, const void* k, const void* v, const void* g_raw
         int rc = check_host_bounds(cu_host, N, T);
         if (rc != KDA_OK) return rc;
     }
+    return KDA_OK;
+}
+
+int common_checks(const void* q, const void* k, const void* v, const void* g_raw,
+                  const void* beta_raw, int raw_bf16, const int32_t* cu_dev,
+                  const int32_t* cu_host, int32_t N, int64_t T, int32_t H, void* out,
+                  float lower_bound, int state_dtype, void* workspace,
+                  size_t workspace_bytes) {
+    int rc = input_checks(q, k, v, g_raw, beta_raw, raw_bf16, cu_dev, cu_host, N, T, H, out,
+                          lower_bound, state_dtype);
+    if (rc != KDA_OK) return rc;
     const size_t need = kda_workspace_size(T, N, H);
     if (need > 0 && (!workspace || workspace_bytes < need))
         return fail(KDA_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed",
@@ -614,6 +626,43 @@ int kda_plan_chunks(const int32_t* cu, int32_t N, int32_t chunk_size, int32_t* c
 }  // extern "C"
 
 namespace {
+// Checks of the paged state pool: the pool, indices and flags are given, the
+// slots can hold the sequences, the slot stride covers a plane and keeps 16-byte
+// alignment, and the pool overlaps no activation.
+int pool_checks(const void* q, const void* k, const void* v, const void* g_raw,
+                const void* beta_raw, int raw_bf16, int32_t num_seqs, int64_t total_tokens,
+                int32_t num_heads, const void* state_cache, int64_t state_stride0,
+                int32_t num_slots, const int32_t* state_indices,
+                const uint8_t* has_initial_state, const void* out, int state_dtype) {
+    if (num_seqs <= 0) return KDA_OK;
+    const int64_t plane = (int64_t)num_heads * kD * kD;
+    if (!state_cache || !state_indices || !has_initial_state)
+        return fail(KDA_ERR_INVALID_ARG,
+                    "state_cache, state_indices and has_initial_state are required");
+    if (num_slots <= 0) return fail(KDA_ERR_INVALID_ARG, "num_slots = %d", num_slots);
+    if (num_slots < num_seqs)
+        return fail(KDA_ERR_INVALID_ARG, "num_slots %d < num_seqs %d (slots are distinct)",
+                    num_slots, num_seqs);
+    if (state_stride0 < plane)
+        return fail(KDA_ERR_INVALID_ARG,
+                    "state_stride0 %lld is smaller than the slot plane H*V*K = %lld",
+                    (long long)state_stride0, (long long)plane);
+    const size_t elt = state_elt(state_dtype);
+    if (!aligned(state_cache, 16) || ((size_t)state_stride0 * elt) % 16 != 0)
+        return fail(KDA_ERR_UNSUPPORTED, "state_cache and its slot stride must be 16-byte aligned");
+    const size_t pool_bytes = ((size_t)(num_slots - 1) * state_stride0 + plane) * elt;
+    Range rp = rng("state_cache", state_cache, pool_bytes);
+    const size_t act = (size_t)total_tokens * num_heads * kD * 2;
+    const size_t relt = raw_bf16 ? 2 : 4;
+    Range others[] = {rng("q", q, act), rng("k", k, act), rng("v", v, act),
+                      rng("g_raw", g_raw, act / 2 * relt),
+                      rng("beta_raw", beta_raw, (size_t)total_tokens * num_heads * relt),
+                      rng("out", out, act)};
+    for (auto& r : others)
+        if (overlaps(rp, r)) return fail(KDA_ERR_INVALID_ARG, "state_cache overlaps %s", r.name);
+    return KDA_OK;
+}
+
 // The paged forward for either raw gate / beta type (raw_bf16: bf16, else fp32).
 int paged_forward(const void* q, const void* k, const void* v, const void* g_raw,
                   const void* beta_raw, int raw_bf16, const int32_t* cu_seqlens,
@@ -626,35 +675,11 @@ int paged_forward(const void* q, const void* k, const void* v, const void* g_raw
     int rc = common_checks(q, k, v, g_raw, beta_raw, raw_bf16, cu_seqlens, cu_seqlens_host,
                            num_seqs, total_tokens, num_heads, out, lower_bound, state_dtype,
                            workspace, workspace_bytes);
+    if (rc == KDA_OK)
+        rc = pool_checks(q, k, v, g_raw, beta_raw, raw_bf16, num_seqs, total_tokens, num_heads,
+                         state_cache, state_stride0, num_slots, state_indices,
+                         has_initial_state, out, state_dtype);
     if (rc != KDA_OK) return rc;
-    const int64_t plane = (int64_t)num_heads * kD * kD;
-    if (num_seqs > 0) {
-        if (!state_cache || !state_indices || !has_initial_state)
-            return fail(KDA_ERR_INVALID_ARG,
-                        "state_cache, state_indices and has_initial_state are required");
-        if (num_slots <= 0) return fail(KDA_ERR_INVALID_ARG, "num_slots = %d", num_slots);
-        if (num_slots < num_seqs)
-            return fail(KDA_ERR_INVALID_ARG, "num_slots %d < num_seqs %d (slots are distinct)",
-                        num_slots, num_seqs);
-        if (state_stride0 < plane)
-            return fail(KDA_ERR_INVALID_ARG,
-                        "state_stride0 %lld is smaller than the slot plane H*V*K = %lld",
-                        (long long)state_stride0, (long long)plane);
-        const size_t elt = state_elt(state_dtype);
-        if (!aligned(state_cache, 16) || ((size_t)state_stride0 * elt) % 16 != 0)
-            return fail(KDA_ERR_UNSUPPORTED,
-                        "state_cache and its slot stride must be 16-byte aligned");
-        const size_t pool_bytes = ((size_t)(num_slots - 1) * state_stride0 + plane) * elt;
-        Range rp = rng("state_cache", state_cache, pool_bytes);
-        const size_t act = (size_t)total_tokens * num_heads * kD * 2;
-        const size_t relt = raw_bf16 ? 2 : 4;
-        Range others[] = {rng("q", q, act), rng("k", k, act), rng("v", v, act),
-                          rng("g_raw", g_raw, act / 2 * relt),
-                          rng("beta_raw", beta_raw, (size_t)total_tokens * num_heads * relt),
-                          rng("out", out, act)};
-        for (auto& r : others)
-            if (overlaps(rp, r)) return fail(KDA_ERR_INVALID_ARG, "state_cache overlaps %s", r.name);
-    }
     StateArgs st{state_cache, state_cache, state_stride0, state_stride0,
                  state_indices, state_indices, has_initial_state, num_slots};
     return run_forward(q, k, v, g_raw, beta_raw, raw_bf16, cu_seqlens, cu_seqlens_host,
@@ -913,8 +938,13 @@ extern "C" int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v
     if (!cu_seqlens || !cu_seqlens_host)
         return fail(KDA_ERR_INVALID_ARG,
                     "kda_chunk_fwd_noalloc needs both cu_seqlens and cu_seqlens_host");
-    if (num_seqs < 0 || total_tokens < 0 || num_heads <= 0)
-        return fail(KDA_ERR_INVALID_ARG, "invalid sizes");
+    int rc = input_checks(q, k, v, g_raw, beta_raw, 0, cu_seqlens, cu_seqlens_host, num_seqs,
+                          total_tokens, num_heads, out, lower_bound, state_dtype);
+    if (rc == KDA_OK)
+        rc = pool_checks(q, k, v, g_raw, beta_raw, 0, num_seqs, total_tokens, num_heads,
+                         state_cache, state_stride0, num_slots, state_indices,
+                         has_initial_state, out, state_dtype);
+    if (rc != KDA_OK) return rc;
     // scratch layout: [workspace][cu | seq_off | chunk_seq | chunk_tok | long | short]
     const int64_t bound = max_chunks(total_tokens, num_seqs);
     const size_t ws_need = kda_workspace_size(total_tokens, num_seqs, num_heads);
@@ -927,30 +957,9 @@ extern "C" int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v
                     "kda_chunk_fwd_noalloc: these sizes need %zu bytes of scratch, the built-in "
                     "scratch holds %llu (KDA_NOALLOC_SCRATCH_BYTES)",
                     need, (unsigned long long)KDA_NOALLOC_SCRATCH_BYTES);
-    void* scratch = nullptr;
-    int rc = noalloc_scratch(&scratch);
+    void* scratch = nullptr;  // 256-byte aligned, and large enough by the check above
+    rc = noalloc_scratch(&scratch);
     if (rc != KDA_OK) return rc;
-    rc = common_checks(q, k, v, g_raw, beta_raw, 0, cu_seqlens, cu_seqlens_host, num_seqs,
-                       total_tokens, num_heads, out, lower_bound, state_dtype, scratch,
-                       (size_t)KDA_NOALLOC_SCRATCH_BYTES);
-    if (rc != KDA_OK) return rc;
-    const int64_t plane = (int64_t)num_heads * kD * kD;
-    if (num_seqs > 0) {
-        if (!state_cache || !state_indices || !has_initial_state)
-            return fail(KDA_ERR_INVALID_ARG,
-                        "state_cache, state_indices and has_initial_state are required");
-        if (num_slots < num_seqs)
-            return fail(KDA_ERR_INVALID_ARG, "num_slots %d < num_seqs %d (slots are distinct)",
-                        num_slots, num_seqs);
-        if (state_stride0 < plane)
-            return fail(KDA_ERR_INVALID_ARG,
-                        "state_stride0 %lld is smaller than the slot plane H*V*K = %lld",
-                        (long long)state_stride0, (long long)plane);
-        const size_t elt = state_elt(state_dtype);
-        if (!aligned(state_cache, 16) || ((size_t)state_stride0 * elt) % 16 != 0)
-            return fail(KDA_ERR_UNSUPPORTED,
-                        "state_cache and its slot stride must be 16-byte aligned");
-    }
     int64_t n_chunks = 0;
     int32_t n_long = 0, max_long = 0;
     for (int32_t n = 0; n < num_seqs; ++n) {

@@ -125,7 +125,9 @@ const char* kernel_name(int i);
 // and marks[i + 1] after kernel i.
 cudaError_t launch_forward(const FwdParams& p, cudaStream_t s, cudaEvent_t* marks);
 // Bit i set when kernel i (launch order) has work for these parameters; a
-// kernel without work is not launched and its timing interval is empty.
+// kernel without work is not launched and its timing interval is empty.  Read
+// after launch_forward: a fused launch the device refused then reads as the
+// two kernels that ran instead.
 unsigned launched_kernels(const FwdParams& p);
 
 // Individual stages (kda_intra.cu, kda_scan.cu, kda_decode.cu).

@@ -54,10 +54,14 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t s, cudaEvent_t* mark
         e = launch_fused(p, s);
         if (e == cudaErrorCooperativeLaunchTooLarge) {
             // the device refused the cooperative launch (and is marked so for
-            // later calls): run the two kernels instead
+            // later calls): run the two kernels instead, re-recording their
+            // marks so the per-kernel times land on kda_intra and kda_scan
             (void)cudaGetLastError();
+            if (marks) cudaEventRecord(marks[0], s);
             e = launch_intra(q, s);
+            if (marks) cudaEventRecord(marks[1], s);
             if (e == cudaSuccess) e = launch_scan(q, scan_groups(n_scan_of(q), q.H, num_sms()), s);
+            if (marks) cudaEventRecord(marks[2], s);
         }
         if (e != cudaSuccess) return e;
     }

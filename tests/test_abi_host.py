@@ -168,6 +168,47 @@ def test_rejects_invalid_arguments(lib, over, code, msg):
     assert msg in lib.kda_last_error(), lib.kda_last_error()
 
 
+def _call_noalloc(lib, a):
+    return lib.kda_chunk_fwd_noalloc(a["q"], a["k"], a["v"], a["g"], a["b"], a["cu"],
+                                     a["cu_host"], a["N"], a["T"], a["H"], a["pool"],
+                                     a["stride0"], a["slots"], a["idx"], a["hs"], a["out"],
+                                     a["lb"], a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code,msg", [
+    (dict(H=0), kda.KDA_ERR_INVALID_ARG, b"num_heads"),
+    (dict(T=-5), kda.KDA_ERR_INVALID_ARG, b"total_tokens"),
+    (dict(stride0=2 * 128 * 128 - 1), kda.KDA_ERR_INVALID_ARG, b"stride0"),
+    (dict(out=BASE + 2 * ACT + 64), kda.KDA_ERR_INVALID_ARG, b"out overlaps v"),
+    (dict(pool=BASE + 64), kda.KDA_ERR_INVALID_ARG, b"state_cache overlaps q"),
+    (dict(pool=BASE + 8 * ACT), kda.KDA_ERR_INVALID_ARG, b"state_cache overlaps out"),
+    (dict(dtype=3), kda.KDA_ERR_UNSUPPORTED, b"state_dtype"),
+    (dict(lb=0.5), kda.KDA_ERR_UNSUPPORTED, b"lower_bound"),
+    (dict(q=BASE + 8), kda.KDA_ERR_UNSUPPORTED, b"aligned"),
+    (dict(pool=None), kda.KDA_ERR_INVALID_ARG, b"required"),
+    (dict(slots=1), kda.KDA_ERR_INVALID_ARG, b"num_slots"),
+    (dict(cu_host=None), kda.KDA_ERR_INVALID_ARG, b"cu_seqlens_host"),
+    (dict(cu=None), kda.KDA_ERR_INVALID_ARG, b"cu_seqlens"),
+])
+def test_noalloc_rejects_invalid_arguments(lib, over, code, msg):
+    """The allocation-free entry point runs the paged entry point's host checks
+    (pool overlaps included) before it touches CUDA."""
+    a = _args(**over)
+    assert _call_noalloc(lib, a) == code
+    assert msg in lib.kda_last_error(), lib.kda_last_error()
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
+    T_big = 1 << 20  # 16 heads of a 1M-token prefill need far more than the scratch
+    cu_host = (ctypes.c_int32 * 2)(0, T_big)
+    act = T_big * 16 * 128 * 2
+    a = _args(N=1, T=T_big, H=16, cu_host=ctypes.addressof(cu_host), q=BASE, k=BASE + act,
+              v=BASE + 2 * act, g=BASE + 3 * act, b=BASE + 5 * act, out=BASE + 6 * act,
+              pool=BASE + 8 * act, stride0=16 * 128 * 128)
+    assert _call_noalloc(lib, a) == kda.KDA_ERR_WORKSPACE
+    assert b"KDA_NOALLOC_SCRATCH_BYTES" in lib.kda_last_error()
+
+
 @pytest.mark.parametrize("bounds,msg", [
     ((1, 40, 100), b"expected 0"),
     ((0, 50, 40), b"decreases"),
