@@ -212,12 +212,14 @@ def _ptr(x: Optional[torch.Tensor]):
     return None if x is None else x.data_ptr()
 
 
-def _host_bounds(cu_seqlens_cpu):
+def _host_bounds(cu_seqlens_cpu, N: int):
     if cu_seqlens_cpu is None:
         return None
     h = torch.as_tensor(cu_seqlens_cpu)
     if h.device.type != "cpu":
         raise ValueError("cu_seqlens_cpu must be a CPU tensor")
+    if h.numel() != N + 1:
+        raise ValueError(f"cu_seqlens_cpu has {h.numel()} bounds, cu_seqlens {N + 1}")
     return h.to(torch.int32).contiguous()
 
 
@@ -225,9 +227,25 @@ def _workspace(workspace, T, N, H, device):
     need = workspace_size(T, N, H)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    if workspace.device != device or not workspace.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous tensor on {device}")
     if workspace.numel() * workspace.element_size() < need:
         raise ValueError(f"workspace too small: {need} bytes needed")
     return workspace
+
+
+def _same_device(device, **tensors) -> None:
+    """Every given tensor lives on `device` (the kernels read them all there)."""
+    for name, x in tensors.items():
+        if x is not None and x.device != device:
+            raise ValueError(f"{name} is on {x.device}, q on {device}")
+
+
+def _per_sequence(x: torch.Tensor, name: str, N: int) -> None:
+    """One entry per sequence, contiguous (the kernels index it by sequence)."""
+    if x.numel() != N or not x.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous tensor of {N} entries, one per "
+                         f"sequence; got shape {tuple(x.shape)}")
 
 
 def _common(q, k, v, g_raw, beta_raw, cu_seqlens, raw_dtypes=(torch.float32,)):
@@ -248,6 +266,9 @@ def _common(q, k, v, g_raw, beta_raw, cu_seqlens, raw_dtypes=(torch.float32,)):
         raise ValueError("g_raw must be [1, T, H, 128] and beta_raw [1, T, H]")
     if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
         raise TypeError("cu_seqlens must be an int32 CUDA tensor")
+    if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1 or not cu_seqlens.is_contiguous():
+        raise ValueError("cu_seqlens must be a contiguous 1-D tensor of N + 1 bounds")
+    _same_device(q.device, k=k, v=v, g_raw=g_raw, beta_raw=beta_raw, cu_seqlens=cu_seqlens)
     return T, H, cu_seqlens.numel() - 1
 
 
@@ -276,7 +297,11 @@ def chunk_fwd(q, k, v, g_raw, beta_raw, cu_seqlens, *, state_cache, state_indice
         hs = hs.view(torch.uint8)
     if hs.dtype != torch.uint8 or not hs.is_cuda:
         raise TypeError("has_initial_state must be a bool/uint8 CUDA tensor")
-    host = _host_bounds(cu_seqlens_cpu)
+    _per_sequence(state_indices, "state_indices", N)
+    _per_sequence(hs, "has_initial_state", N)
+    _same_device(q.device, out=out, state_cache=state_cache, state_indices=state_indices,
+                 has_initial_state=hs)
+    host = _host_bounds(cu_seqlens_cpu, N)
     ws = _workspace(workspace, T, N, H, q.device)
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
     fn = lib.kda_chunk_fwd_raw_bf16 if g_raw.dtype == torch.bfloat16 else lib.kda_chunk_fwd
@@ -311,9 +336,15 @@ def chunk_fwd_dense(q, k, v, g_raw, beta_raw, cu_seqlens, *, final_state, out,
         if tuple(initial_state.shape) != (N, H, 128, 128):
             raise ValueError("initial_state must be [N, H, 128, 128]")
     hs = has_initial_state
-    if hs is not None and hs.dtype == torch.bool:
-        hs = hs.view(torch.uint8)
-    host = _host_bounds(cu_seqlens_cpu)
+    if hs is not None:
+        if hs.dtype == torch.bool:
+            hs = hs.view(torch.uint8)
+        if hs.dtype != torch.uint8 or not hs.is_cuda:
+            raise TypeError("has_initial_state must be a bool/uint8 CUDA tensor")
+        _per_sequence(hs, "has_initial_state", N)
+    _same_device(q.device, out=out, final_state=final_state, initial_state=initial_state,
+                 has_initial_state=hs)
+    host = _host_bounds(cu_seqlens_cpu, N)
     ws = _workspace(workspace, T, N, H, q.device)
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
     rc = lib.kda_chunk_fwd_dense(
