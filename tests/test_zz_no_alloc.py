@@ -10,7 +10,6 @@ covers the array keeping the previous call's contents.
 Kept in a file of its own, collected last, so that a run that stops at the
 first failure has run every other test before this one.
 """
-import ctypes
 
 import numpy as np
 import pytest
@@ -58,15 +57,3 @@ def test_noalloc_matches_chunk_fwd_two_calls(lengths, H, dt):
         # unselected slots and the stride padding keep their bytes
         assert torch.equal(new.storage.cpu().view(torch.uint8), ref.storage.cpu().view(torch.uint8))
 
-
-def test_noalloc_rejects_oversized_call():
-    """A call whose scratch need exceeds the built-in array fails with a clear
-    workspace error before any GPU work."""
-    lib = kda.load_library()
-    T, H = 1 << 20, 12  # far beyond the built-in scratch
-    cu_host = torch.tensor([0, T], dtype=torch.int32)
-    rc = lib.kda_chunk_fwd_noalloc(None, None, None, None, None, 1 << 40, cu_host.data_ptr(),
-                                   1, T, H, None, H * 128 * 128, 1, None, None, None, -5.0, 0,
-                                   None)
-    assert rc == kda.KDA_ERR_WORKSPACE
-    assert b"KDA_NOALLOC_SCRATCH_BYTES" in lib.kda_last_error()
