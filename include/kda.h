@@ -29,9 +29,12 @@
  * thing: a cache of per-bounds metadata (device buffers plus a pinned staging
  * ring), kept for the life of the process or until kda_release_cache().
  *
- * Errors.  Every entry point returns KDA_OK (0) or a negative code; nothing
- * is validated on the device (no synchronising index checks).
- * kda_last_error() returns a message for the calling thread's last failure.
+ * Errors.  Every entry point returns KDA_OK (0) or a negative code from checks
+ * made on the host before any work is enqueued.  Nothing is checked on the
+ * device in a way that synchronises: the kernels compare state indices with
+ * num_slots where they use them and record a bad one in a status word that
+ * kda_check_status() reads afterwards.  kda_last_error() returns a message for
+ * the calling thread's last failure.
  *
  * Streams.  All work is enqueued on `stream` (a cudaStream_t).  With host
  * bounds the call makes no synchronising CUDA call; without them it makes
@@ -112,7 +115,7 @@ KDA_API size_t kda_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_
  *   has_initial_state device uint8 [num_seqs]: 0 starts the sequence from a
  *                    zero state and never reads its slot.
  *   out              device bf16 [total_tokens][num_heads][128], fully written;
- *                    must not overlap v or the pool.
+ *                    must not overlap any input or the pool.
  *   lower_bound      gate lower bound (e.g. -5); must lie in [-64, 0].
  *   workspace        device scratch of at least kda_workspace_size() bytes,
  *                    256-byte aligned; contents on entry do not matter.
