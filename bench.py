@@ -14,6 +14,11 @@ needed between steps.
 Run:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 With N > 1 it is launched by torch.distributed.run, one rank per GPU; each rank
 runs an independent replica of the workload (the op has no exchange step).
+
+Extra measurements: --workload picks another named workload, --meta-miss times
+calls whose bounds are new to the metadata cache, --gather-arm times the dense
+pipeline (gather the selected slots, dense forward, scatter, out copy) that
+reading and writing the pool in-kernel replaces.
 """
 from __future__ import annotations
 
@@ -62,6 +67,9 @@ def parse():
     ap.add_argument("--workload", default="prefill_16k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--gather-arm", action="store_true",
+                    help="also time the dense pipeline in-kernel paging replaces (gather, "
+                         "dense forward, scatter, out copy) beside the paged call")
     ap.add_argument("--meta-miss", action="store_true",
                     help="also time calls whose bounds are new to the metadata cache")
     ap.add_argument("--clock-seconds", type=float, default=1.5,
@@ -242,28 +250,32 @@ def run_ours(args, rank, world):
     # own and L2 is flushed (a 256 MB write) between steps, outside the events.
     step_bytes = BYTES_PER_TOKHEAD * T * H + 2 * 74240 * H * (T // 64 + N) + state_bytes(w)
     flush = step_bytes < 2 * L2_BYTES
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    barrier()
-    if flush:
-        scratch = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-        for a, z in ev:
-            scratch.zero_()
-            a.record(stream)
-            step()
-            z.record(stream)
-        torch.cuda.synchronize(dev)
+    scratch = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush else None
+
+    def time_steps(fn):
+        """Milliseconds of args.steps calls of fn, CUDA events on the launching
+        stream; with the flush, each call is timed alone after an L2 flush."""
         barrier()
-        ms_total = sum(a.elapsed_time(z) for a, z in ev)
-    else:
+        if flush:
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            for a, z in ev:
+                scratch.zero_()
+                a.record(stream)
+                fn()
+                z.record(stream)
+            barrier()
+            return sum(a.elapsed_time(z) for a, z in ev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(args.steps):
-            step()
+            fn()
         e1.record(stream)
         barrier()
-        ms_total = e0.elapsed_time(e1)
+        return e0.elapsed_time(e1)
+
+    ms_total = time_steps(step)
     # keep the GPU busy with the same step until the clock sampling spans
     # enough samples (the timed region itself can be shorter than the
     # sampling period)
@@ -327,6 +339,38 @@ def run_ours(args, rank, world):
     # so step i + 1's upload and step i - 1's read-back overlap step i's forward
     # (the forwards themselves stay in order: each updates the state pool).
     e2e = None
+    # the dense pipeline that in-kernel paging replaces, on the same inputs:
+    # gather the selected slots into a dense tensor, run the dense entry point,
+    # scatter the final states back, copy out from the kernel's own buffer
+    gather_arm = None
+    if args.gather_arm:
+        if w.g_raw.dtype != torch.float32:
+            gather_arm = {"unavailable": "the dense entry point takes fp32 raw gate and beta"}
+        else:
+            idx_l = idx.long()
+            dense_in = torch.empty((N, H, 128, 128), dtype=pool.dtype, device=dev)
+            dense_out = torch.empty_like(dense_in)
+            out_k = torch.empty_like(out)
+
+            def gather_step():
+                torch.index_select(pool, 0, idx_l, out=dense_in)
+                kda.chunk_fwd_dense(q, k, v, g, b, cu, initial_state=dense_in,
+                                    has_initial_state=hs, final_state=dense_out, out=out_k,
+                                    lower_bound=w.lower_bound, cu_seqlens_cpu=w.cu_seqlens,
+                                    workspace=ws)
+                pool.index_copy_(0, idx_l, dense_out)
+                out.copy_(out_k)
+
+            for _ in range(args.warmup):
+                gather_step()
+            ms_gather = max_over_ranks(time_steps(gather_step)) / args.steps
+            ms_paged = max_over_ranks(time_steps(step)) / args.steps  # re-timed beside it
+            gather_arm = {
+                "us_per_call": ms_gather * 1e3, "paged_us_per_call": ms_paged * 1e3,
+                "paging_saves_us": (ms_gather - ms_paged) * 1e3,
+                "steps": "slots gathered into a dense tensor (index_select), dense entry "
+                         "point, final states scattered back (index_copy_), out copied"}
+
     if not args.no_e2e:
         names = ("q", "k", "v", "g_raw", "beta_raw", "cu", "idx", "hs")
         host = dict(q=w.q, k=w.k, v=w.v, g_raw=w.g_raw, beta_raw=w.beta_raw,
@@ -434,6 +478,7 @@ def run_ours(args, rank, world):
         "clocks": clocks,
         "e2e": e2e,
         **({"metadata_miss": meta_miss} if meta_miss else {}),
+        **({"gather_arm": gather_arm} if gather_arm else {}),
         "gpu_launches": n_launch_per_step * args.steps,
     }
     if world == 1 and not args.no_cpu_baseline:
