@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(scan::kScanThreads, 1) kda_scan_mma(FwdParams 
 // S Phi + N (Phi = product of its M_c, N = its state from a zero start):
 //   pass A  per segment but the last, in parallel: N from a zero state, and Phi
 //           as the walk of the K identity rows with u = 0;
-//   combine per (pair, 16 value rows), in order: S_start(s + 1) = S_start(s) Phi_s + N_s
+//   combine per (pair, 4 value rows), in order: S_start(s + 1) = S_start(s) Phi_s + N_s
 //           (fp32), S_start(0) the pool state;
 //   pass B  per segment, in parallel: the walk from S_start(s), writing the
 //           outputs and, for the last segment, the pool.
@@ -104,55 +104,89 @@ __global__ void __launch_bounds__(scan::kScanThreads, 1) kda_scan_seg(FwdParams 
     scan::scan_walk<2>(p, smem, n, h, z, R);
 }
 
-// S_start(s + 1) = S_start(s) Phi_s + N_s for value rows 16 blockIdx.y .. of pair
-// blockIdx.x; thread t: row t / 16, keys 8 (t % 16) .. + 7.
-constexpr int kCombThreads = 256;
-constexpr int kCombSmem = (128 * 128 + 16 * 129) * 4;
+// S_start(s + 1) = S_start(s) Phi_s + N_s for kCombRows value rows (blockIdx.y) of
+// pair blockIdx.x, one key channel k per thread: acc_r += S_start[r][j] Phi_s[j][k]
+// over j, the rows of S_start read as one broadcast float4 per j and Phi_s as one
+// coalesced row.  The transitions arrive by bulk copies into two shared buffers,
+// the next one copied while the current step computes (they depend only on pass A).
+constexpr int kCombRows = 4;
+constexpr int kCombThreads = kD;
+constexpr uint32_t kPlaneBytes = (uint32_t)(kPlane * sizeof(float));
+constexpr int kCombSmem = (int)(2 * kPlaneBytes + kD * kCombRows * sizeof(float) + 2 * sizeof(uint64_t));
+static_assert(kCombRows == 4, "the rows of S_start are read as one float4");
+
 __global__ void __launch_bounds__(kCombThreads) kda_scan_combine(FwdParams p, int P, int L) {
-    extern __shared__ float csm[];
-    float* phi = csm;               // [128][128]
-    float* S = csm + 128 * 128;     // [16][129]
-    const int pair = blockIdx.x, z = blockIdx.y, t = threadIdx.x;
+    using namespace dev;
+    extern __shared__ __align__(128) uint8_t csm[];
+    float* phi = reinterpret_cast<float*>(csm);                        // [2][K][K]
+    float* st = phi + 2 * kPlane;                                      // [K][kCombRows]: S_start^T
+    uint64_t* bar = reinterpret_cast<uint64_t*>(st + kD * kCombRows);  // one per buffer
+    const int pair = blockIdx.x, v0 = kCombRows * (int)blockIdx.y, k = threadIdx.x;
     int n, h, Pn;
     seg_pair(p, pair, L, n, h, Pn);
-    if (Pn < 2) return;
-    const int r = t >> 4, k0 = (t & 15) * 8, v = 16 * z + r;
-    // S_start(0): the pool row (zero without an initial state or for a slot outside the pool)
+    const int steps = Pn - 1;
+    if (steps < 1) return;
+    float* base = seg_planes(p, P, pair);
+    if (k == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
+        for (int b = 0; b < 2 && b < steps; ++b) {
+            mbar_arrive_expect_tx(&bar[b], kPlaneBytes);
+            bulk_g2s(phi + b * kPlane, base + (size_t)b * kPlane, kPlaneBytes, &bar[b]);
+        }
+    }
+    // S_start(0): the pool rows (zero without an initial state or for a slot outside the pool)
     bool init = p.has_init ? (p.has_init[n] != 0) : (p.st_in != nullptr);
     const int64_t slot = p.st_in_idx ? p.st_in_idx[n] : n;
     if (p.num_slots > 0 && (slot < 0 || slot >= p.num_slots)) init = false;
-    const size_t row = (size_t)slot * p.st_in_stride + ((size_t)h * kD + v) * kD;
+    float s0[kCombRows];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) S[r * 129 + k0 + e] = init ? scan::load_state(p.st_in, p.st_dtype, row + k0 + e) : 0.f;
-    float* base = seg_planes(p, P, pair);
-    for (int sg = 0; sg < Pn - 1; ++sg) {
-        const float4* ph = reinterpret_cast<const float4*>(base + (size_t)sg * kPlane);
-        for (int i = t; i < 128 * 128 / 4; i += kCombThreads) reinterpret_cast<float4*>(phi)[i] = ph[i];
-        const float* nb = base + (size_t)(P - 1 + sg) * kPlane + (size_t)v * kD + k0;
-        float acc[8];
+    for (int r = 0; r < kCombRows; ++r)
+        s0[r] = init ? scan::load_state(p.st_in, p.st_dtype,
+                                        (size_t)slot * p.st_in_stride +
+                                            ((size_t)h * kD + v0 + r) * kD + k)
+                     : 0.f;
+    *reinterpret_cast<float4*>(st + k * kCombRows) = make_float4(s0[0], s0[1], s0[2], s0[3]);
+    __syncthreads();  // barriers initialised, S_start(0) in place
+
+    for (int sg = 0; sg < steps; ++sg) {
+        const int b = sg & 1;
+        const uint32_t par = (uint32_t)(sg >> 1) & 1;
+        const float* nb = base + (size_t)(P - 1 + sg) * kPlane + (size_t)v0 * kD + k;
+        float acc[kCombRows];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = nb[e];
-        __syncthreads();
-        for (int j = 0; j < 128; ++j) {
-            const float a = S[r * 129 + j];
-            const float4 p0 = *reinterpret_cast<const float4*>(phi + j * 128 + k0);
-            const float4 p1 = *reinterpret_cast<const float4*>(phi + j * 128 + k0 + 4);
-            acc[0] = fmaf(a, p0.x, acc[0]);
-            acc[1] = fmaf(a, p0.y, acc[1]);
-            acc[2] = fmaf(a, p0.z, acc[2]);
-            acc[3] = fmaf(a, p0.w, acc[3]);
-            acc[4] = fmaf(a, p1.x, acc[4]);
-            acc[5] = fmaf(a, p1.y, acc[5]);
-            acc[6] = fmaf(a, p1.z, acc[6]);
-            acc[7] = fmaf(a, p1.w, acc[7]);
+        for (int r = 0; r < kCombRows; ++r) acc[r] = nb[(size_t)r * kD];
+        if (!__syncthreads_and(mbar_wait(&bar[b], par))) {
+            // report, and let this CTA's copies in flight land before it leaves
+            if (k == 0) {
+                if (p.status) atomicOr(p.status, 1);
+                mbar_wait(&bar[b], par);
+                if (sg + 1 < steps) mbar_wait(&bar[b ^ 1], (uint32_t)((sg + 1) >> 1) & 1);
+            }
+            return;
         }
-        __syncthreads();  // S and phi are read
-        float* out = base + (size_t)(2 * (P - 1) + sg) * kPlane + (size_t)v * kD + k0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            S[r * 129 + k0 + e] = acc[e];
-            out[e] = acc[e];
+        const float* ph = phi + b * kPlane;
+#pragma unroll 8
+        for (int j = 0; j < kD; ++j) {
+            const float4 s = *reinterpret_cast<const float4*>(st + j * kCombRows);
+            const float f = ph[j * kD + k];
+            acc[0] = fmaf(s.x, f, acc[0]);
+            acc[1] = fmaf(s.y, f, acc[1]);
+            acc[2] = fmaf(s.z, f, acc[2]);
+            acc[3] = fmaf(s.w, f, acc[3]);
         }
+        __syncthreads();  // every thread is done with st and with buffer b
+        if (k == 0 && sg + 2 < steps) {
+            fence_proxy_async();
+            mbar_arrive_expect_tx(&bar[b], kPlaneBytes);
+            bulk_g2s(phi + b * kPlane, base + (size_t)(sg + 2) * kPlane, kPlaneBytes, &bar[b]);
+        }
+        float* out = base + (size_t)(2 * (P - 1) + sg) * kPlane + (size_t)v0 * kD + k;
+#pragma unroll
+        for (int r = 0; r < kCombRows; ++r) out[(size_t)r * kD] = acc[r];
+        *reinterpret_cast<float4*>(st + k * kCombRows) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        __syncthreads();  // S_start(sg + 1) in place
     }
 }
 
@@ -179,7 +213,7 @@ cudaError_t launch_scan_segmented(const FwdParams& p, int P, int L, cudaStream_t
     kda_scan_seg<false><<<pairs * (P - 1) * 2 * walks, scan::kScanThreads, Lyt::kTotal, s>>>(p, P, L);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    kda_scan_combine<<<dim3(pairs, walks), kCombThreads, kCombSmem, s>>>(p, P, L);
+    kda_scan_combine<<<dim3(pairs, kD / kCombRows), kCombThreads, kCombSmem, s>>>(p, P, L);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     kda_scan_seg<true><<<pairs * P * walks, scan::kScanThreads, Lyt::kTotal, s>>>(p, P, L);
