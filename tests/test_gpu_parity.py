@@ -1,7 +1,6 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle, on
 small cases that span several chunks with ragged tails, on the named serving
 workloads (sampled heads at full size), and on the edge cases of the method."""
-import numpy as np
 import pytest
 import torch
 

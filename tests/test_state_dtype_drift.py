@@ -11,7 +11,6 @@ bf16 storage of an fp32-accumulated state, and whether the error grows with
 sequence length); here it also pins that the drift stays inside the forward's
 tolerance for each pool type.
 """
-import numpy as np
 import pytest
 import torch
 
