@@ -100,6 +100,21 @@ def check_brute_force(fwd, seed=0, K=6, V=4, H=2, lb=-5.0):
     assert rel(fin, bfin) < 1e-12, rel(fin, bfin)
 
 
+def check_brute_force_wide(fwd, seed=7, K=24, V=40, H=2, lb=-5.0):
+    """The unrolled form with more value rows than one work block of the oracle
+    holds (16), and a ragged last block: every row's inputs, initial state,
+    output and final state land at its own index."""
+    rng = np.random.default_rng(seed)
+    c = rand_case(rng, [4, 0, 3], H, K, V)
+    flags = np.array([1, 0, 1], np.uint8)
+    out, fin = fwd(c["q"], c["k"], c["v"], c["g_raw"], c["beta_raw"], c["cu"],
+                   c["init"], flags, lb)
+    bo, bfin = brute_force(c["q"], c["k"], c["v"], c["g_raw"], c["beta_raw"],
+                           c["cu"], c["init"], flags, lb)
+    assert rel(out, bo) < 1e-12, rel(out, bo)
+    assert rel(fin, bfin) < 1e-12, rel(fin, bfin)
+
+
 def check_noop_tokens(fwd, K=6, V=4, H=2, lb=-5.0):
     """raw gate = raw beta = -inf gives g = 0 and b = 0: the state is carried
     unchanged and every output is S_0 q^."""
@@ -243,7 +258,8 @@ def check_sequence_independence(fwd, K=6, V=4, H=2, lb=-5.0):
 
 
 ALL_CHECKS = [
-    check_brute_force, check_noop_tokens, check_pure_decay, check_single_token,
+    check_brute_force,
+    check_brute_force_wide, check_noop_tokens, check_pure_decay, check_single_token,
     check_delta_write, check_zero_init_flag, check_empty_sequence,
     check_row_permutation, check_scale_invariance, check_split_call,
     check_sequence_independence,

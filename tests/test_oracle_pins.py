@@ -111,6 +111,28 @@ MUTANTS = {
     "reads_unflagged_init": ("if (has_init && has_init[n]) {", "if (init) {"),
     "write_uses_q": ("for (int c = 0; c < K; ++c) s[c] += d * kn[c];",
                      "for (int c = 0; c < K; ++c) s[c] += d * qn[c] * sqrt((double)K);"),
+    "decay_after_write": [
+        ("for (int c = 0; c < K; ++c) s[c] *= dec[c];", "/* no decay before the write */"),
+        ("for (int c = 0; c < K; ++c) s[c] += d * kn[c];",
+         "for (int c = 0; c < K; ++c) s[c] += d * kn[c];\n"
+         "for (int c = 0; c < K; ++c) s[c] *= dec[c];")],
+    "output_before_write": [
+        ("const double d = beta * (v[tv + v0 + r] - sk);",
+         "double o0 = 0.0; for (int c = 0; c < K; ++c) o0 += s[c] * qn[c];\n"
+         "const double d = beta * (v[tv + v0 + r] - sk);"),
+        ("out[tv + v0 + r] = o;", "out[tv + v0 + r] = o0; (void)o;")],
+    "beta_on_erase_only": ("const double d = beta * (v[tv + v0 + r] - sk);",
+                           "const double d = v[tv + v0 + r] - beta * sk;"),
+    "lower_bound_ignored": ("decay[c] = exp(lower_bound * sigmoid(g_raw[c]));",
+                            "decay[c] = exp(-sigmoid(g_raw[c]));"),
+    "last_token_skipped": ("for (int64_t t = cu[n]; t < cu[n + 1]; ++t) {",
+                           "for (int64_t t = cu[n]; t + 1 < cu[n + 1]; ++t) {"),
+    "init_ignored": ("if (has_init && has_init[n]) {", "if (0 && has_init && has_init[n]) {"),
+    "row_block_offset_dropped": [
+        ("v[tv + v0 + r]", "v[tv + r]"),
+        ("out[tv + v0 + r] = o;", "out[tv + r] = o;"),
+        ("const size_t sbase = ((size_t)n * H + h) * plane + (size_t)v0 * K;",
+         "const size_t sbase = ((size_t)n * H + h) * plane;")],
 }
 
 
@@ -126,11 +148,13 @@ def test_pins_catch_mutant(name, mutant_dir):
     if shutil.which("gcc") is None:
         pytest.skip("gcc not available")
     src = open(oracle._SRC).read()
-    old, new = MUTANTS[name]
-    assert old in src, f"mutation anchor for {name} no longer in the oracle source"
+    edits = MUTANTS[name]
+    for old, new in ([edits] if isinstance(edits, tuple) else edits):
+        assert src.count(old) == 1, f"mutation anchor for {name} not found once in the source"
+        src = src.replace(old, new, 1)
     msrc = os.path.join(mutant_dir, f"{name}.c")
     with open(msrc, "w") as f:
-        f.write(src.replace(old, new, 1))
+        f.write(src)
     mlib = os.path.join(mutant_dir, f"lib{name}.so")
     oracle.build(msrc, mlib)
     lib = oracle.load(mlib)
