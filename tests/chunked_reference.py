@@ -66,3 +66,67 @@ def forward(q, k, v, g_raw, beta_raw, cu, init, flags, lb, C=64, eps=1e-6):
                 S = S * tl["gamma"][None, :] + U.T @ tl["kg"]
             fin[n, h] = S
     return out, fin
+
+
+# ---------------------------------------------------------------------------
+# Segmented walk.  Each chunk maps the state affinely, S -> S M_c + N_c with
+# M_c = Diag(gamma) - w^T kg and N_c = u^T kg, so a run of chunks maps its start
+# state S to S Phi + N: Phi is the walk of the K identity rows with u = 0, N the
+# walk of a zero state.  The segments' (Phi, N) are independent of one another
+# and of the incoming state; chaining S_start(s + 1) = S_start(s) Phi_s + N_s and
+# walking each segment from its start state gives the serial walk's outputs and
+# final state.  (ROCm/aiter PR #4741, "Optimizations Applied", splits the state
+# walk of long sequences into segments; this composition is the build's own.)
+# ---------------------------------------------------------------------------
+
+def _padded_tiles(q, k, v, g_raw, beta_raw, lb, t_begin, t_end, h, C, eps):
+    """(first token, valid rows, tiles) of the chunks of tokens t_begin..t_end-1."""
+    tiles = []
+    for t0 in range(t_begin, t_end, C):
+        L = min(C, t_end - t0)
+
+        def pad(x, fill=0.0):
+            return np.concatenate([x, np.full((C - L,) + x.shape[1:], fill)]) if L < C else x
+
+        tl = chunk_tiles(pad(q[t0:t0 + L, h]), pad(k[t0:t0 + L, h]), pad(v[t0:t0 + L, h]),
+                         pad(g_raw[t0:t0 + L, h], -np.inf), pad(beta_raw[t0:t0 + L, h], -np.inf),
+                         lb, eps)
+        tiles.append((t0, L, tl))
+    return tiles
+
+
+def _walk(S, tiles, zero_u=False, out=None, h=None):
+    """The serial walk over `tiles` from state S (rows of any count); with
+    zero_u the chunks' u are taken as 0; with `out` the outputs are written."""
+    for t0, L, tl in tiles:
+        u = np.zeros((tl["w"].shape[0], S.shape[0])) if zero_u else tl["u"]
+        U = u - tl["w"] @ S.T
+        if out is not None:
+            out[t0:t0 + L, h] = (tl["qg"] @ S.T + tl["Aqk"] @ U)[:L]
+        S = S * tl["gamma"][None, :] + U.T @ tl["kg"]
+    return S
+
+
+def forward_segmented(q, k, v, g_raw, beta_raw, cu, init, flags, lb, C=64, seg_chunks=2,
+                      eps=1e-6):
+    """The chunkwise forward with each sequence's walk cut into segments of
+    seg_chunks chunks: pass A (Phi, N of every segment but the last), the chain of
+    segment start states, pass B (every segment from its start state)."""
+    T_, H, K = q.shape
+    V = v.shape[2]
+    N = len(cu) - 1
+    out = np.zeros((T_, H, V))
+    fin = np.zeros((N, H, V, K))
+    for n in range(N):
+        for h in range(H):
+            tiles = _padded_tiles(q, k, v, g_raw, beta_raw, lb, cu[n], cu[n + 1], h, C, eps)
+            segs = [tiles[i:i + seg_chunks] for i in range(0, len(tiles), seg_chunks)] or [[]]
+            phi = [_walk(np.eye(K), sg, zero_u=True) for sg in segs[:-1]]
+            nst = [_walk(np.zeros((V, K)), sg) for sg in segs[:-1]]
+            starts = [init[n, h].copy() if flags[n] else np.zeros((V, K))]
+            for s in range(len(segs) - 1):
+                starts.append(starts[s] @ phi[s] + nst[s])
+            for s, sg in enumerate(segs):
+                S = _walk(starts[s], sg, out=out, h=h)
+            fin[n, h] = S
+    return out, fin
