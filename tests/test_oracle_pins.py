@@ -144,6 +144,7 @@ def mutant_dir():
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")  # a planted mistake may overflow
 def test_pins_catch_mutant(name, mutant_dir):
     if shutil.which("gcc") is None:
         pytest.skip("gcc not available")
