@@ -130,3 +130,43 @@ def forward_segmented(q, k, v, g_raw, beta_raw, cu, init, flags, lb, C=64, seg_c
                 S = _walk(starts[s], sg, out=out, h=h)
             fin[n, h] = S
     return out, fin
+
+
+# ---------------------------------------------------------------------------
+# Bounded construction of the decay factors e^{G_i - G_j} (j <= i) of one chunk,
+# as the tensor-core intra kernel forms them: the chunk is cut into 16-row
+# blocks; with a = e^g per token and channel, P_i the product of a over block
+# rows up to i and E_B a block's total, a pair in blocks J < I is
+# P_i * (E_{J+1} ... E_{I-1}) * (E_J / P_j) and a pair inside one block P_i / P_j.
+# Every factor of the off-diagonal form is <= 1, so nothing overflows whatever
+# the decay; the diagonal quotient needs P >= ~e^-87 in fp32, which holds while
+# a block's 16 tokens decay by at most 80 nats (lower_bound >= -5).
+# ---------------------------------------------------------------------------
+
+def bounded_decay_pairs(g_raw, lb, dtype=np.float32, block=16):
+    """[C, C, K] factors e^{G_i - G_j} for j <= i (0 above the diagonal),
+    evaluated in `dtype` by the bounded construction."""
+    C, K = g_raw.shape
+    a = np.exp((lb * _sig(g_raw.astype(np.float64))).astype(dtype)).astype(dtype)
+    nb = C // block
+    P = np.empty_like(a)
+    E = np.empty((nb, K), dtype)
+    for B in range(nb):
+        acc = np.ones(K, dtype)
+        for r in range(block):
+            acc = (acc * a[B * block + r]).astype(dtype)
+            P[B * block + r] = acc
+        E[B] = acc
+    out = np.zeros((C, C, K), dtype)
+    for i in range(C):
+        I = i // block
+        for j in range(i + 1):
+            J = j // block
+            if I == J:
+                out[i, j] = P[i] / P[j]
+            else:
+                mid = np.ones(K, dtype)
+                for B in range(J + 1, I):
+                    mid = (mid * E[B]).astype(dtype)
+                out[i, j] = P[i] * mid * (E[J] / P[j])
+    return out

@@ -37,3 +37,28 @@ def test_segmented_walk_equals_token_recurrence(C, seg_chunks, gate_scale, oracl
                                     seg_chunks=seg_chunks)
     assert pins.rel(o2, o1) < 1e-10
     assert pins.rel(f2, f1) < 1e-10
+
+
+@pytest.mark.parametrize("gate_scale,offset", [(1.0, 0.0), (1.0, 8.0), (4.0, 30.0)])
+def test_bounded_decay_construction(gate_scale, offset):
+    """The intra kernel's block-factored decay factors equal e^{G_i - G_j} (fp32
+    against fp64, relative to each factor), stay finite at saturated gates
+    (lower_bound -5 and raw gates of +8 and beyond: ~5 nats per token, 320 per
+    chunk), where the two-exponential form e^{G_i} e^{-G_j} overflows in fp32."""
+    rng = np.random.default_rng(int(offset) + 3)
+    C, K, lb = 64, 32, -5.0
+    g_raw = rng.standard_normal((C, K)) * gate_scale + offset
+    g = lb / (1.0 + np.exp(-g_raw))
+    G = np.cumsum(g, axis=0)
+    exact = np.tril(np.ones((C, C)))[:, :, None] * np.exp(
+        np.minimum(G[:, None, :] - G[None, :, :], 0.0))
+    got = cref.bounded_decay_pairs(g_raw, lb).astype(np.float64)
+    assert np.isfinite(got).all()
+    tiny = exact > 1e-30  # below that fp32 flushes; the kernel loses only such values
+    assert np.all(np.abs(got[tiny] - exact[tiny]) <= 2e-5 * exact[tiny])
+    assert np.all(got[~tiny] < 1e-29)
+    if offset >= 8.0:
+        with np.errstate(over="ignore", invalid="ignore"):
+            Gf = G.astype(np.float32)
+            naive = np.exp(Gf)[:, None, :] * np.exp(-Gf)[None, :, :]
+        assert not np.isfinite(naive[np.tril(np.ones((C, C), bool))]).all()
