@@ -170,3 +170,100 @@ def bounded_decay_pairs(g_raw, lb, dtype=np.float32, block=16):
                     mid = (mid * E[B]).astype(dtype)
                 out[i, j] = P[i] * mid * (E[J] / P[j])
     return out
+
+
+# ---------------------------------------------------------------------------
+# Operand-rounding model of the kernels' precision choices.  Every tensor-core
+# operand is rounded to the type it is stored in; sums are exact (fp64), since
+# fp32 accumulation adds far less error than 10- or 7-bit operand mantissas.
+#   "kernel": diagonal 16-row blocks of A_qk / A_kk from tf32 operands, every
+#             other operand fp16 (off-diagonal factors, the middle-block decay
+#             table, T's off-diagonal blocks, w, u, qg, kg, A_qk, U and the
+#             state operand), the state master copy and gamma unrounded, out bf16;
+#   "bf16":   the same with every one of those operands in bf16;
+#   "diag_bf16": the kernel's choice except for bf16 diagonal blocks.
+# ---------------------------------------------------------------------------
+
+def _round_bits(x, drop):
+    """Round-to-nearest-even of fp32 values to (23 - drop) mantissa bits."""
+    f = np.asarray(x, np.float32).copy()
+    u = f.view(np.uint32)
+    bias = np.uint32((1 << (drop - 1)) - 1) + ((u >> np.uint32(drop)) & np.uint32(1))
+    u[:] = (u + bias) & ~np.uint32((1 << drop) - 1)
+    return f.astype(np.float64)
+
+
+def rnd(x, kind):
+    if kind == "fp16":
+        return np.asarray(x, np.float64).astype(np.float16).astype(np.float64)
+    if kind == "tf32":
+        return _round_bits(x, 13)
+    if kind == "bf16":
+        return _round_bits(x, 16)
+    return np.asarray(x, np.float64)
+
+
+def forward_rounded(q, k, v, g_raw, beta_raw, cu, lb, prec="kernel", C=64, block=16,
+                    eps=1e-6):
+    """Outputs [T, H, V] of zero-initial-state sequences under the rounding model."""
+    diag_t, op_t = {"kernel": ("tf32", "fp16"), "bf16": ("bf16", "bf16"),
+                    "diag_bf16": ("bf16", "fp16")}[prec]
+    T_, H, K = q.shape
+    V = v.shape[2]
+    out = np.zeros((T_, H, V))
+    nb = C // block
+    blk = np.arange(C) // block
+    for n in range(len(cu) - 1):
+        for h in range(H):
+            S = np.zeros((V, K))
+            for t0 in range(cu[n], cu[n + 1], C):
+                L = min(C, cu[n + 1] - t0)
+                qq, kk, vv = (np.zeros((C, K)), np.zeros((C, K)), np.zeros((C, V)))
+                gg = np.full((C, K), -np.inf)
+                bb = np.full(C, -np.inf)
+                qq[:L], kk[:L], vv[:L] = q[t0:t0 + L, h], k[t0:t0 + L, h], v[t0:t0 + L, h]
+                gg[:L], bb[:L] = g_raw[t0:t0 + L, h], beta_raw[t0:t0 + L, h]
+                qn = qq / np.sqrt((qq * qq).sum(1, keepdims=True) + eps) / np.sqrt(K)
+                kn = kk / np.sqrt((kk * kk).sum(1, keepdims=True) + eps)
+                g = lb * _sig(gg)
+                b = _sig(bb)
+                G = np.cumsum(g, axis=0)
+                a = np.exp(g)
+                P = np.empty_like(a)
+                E = np.empty((nb, K))
+                for B in range(nb):
+                    P[B * block:(B + 1) * block] = np.cumprod(a[B * block:(B + 1) * block], axis=0)
+                    E[B] = P[(B + 1) * block - 1]
+                R = E[blk] / P                      # E_J / P_j
+                Aqk = np.zeros((C, C))
+                Akk = np.zeros((C, C))
+                for I in range(nb):
+                    ri = slice(I * block, (I + 1) * block)
+                    for J in range(I + 1):
+                        rj = slice(J * block, (J + 1) * block)
+                        if I == J:
+                            right = rnd(kn[rj] / P[rj], diag_t)
+                            lq, lk = rnd(qn[ri] * P[ri], diag_t), rnd(kn[ri] * P[ri], diag_t)
+                        else:
+                            mid = rnd(np.prod(E[J + 1:I], axis=0), op_t)
+                            right = rnd(kn[rj] * R[rj], op_t)
+                            lq = rnd(rnd(qn[ri] * P[ri], op_t) * mid, op_t)
+                            lk = rnd(rnd(kn[ri] * P[ri], op_t) * mid, op_t)
+                        Aqk[ri, rj] = lq @ right.T
+                        Akk[ri, rj] = b[ri, None] * (lk @ right.T)
+                Aqk = np.tril(Aqk)
+                Akk = np.tril(Akk, -1)
+                off = blk[:, None] != blk[None, :]
+                Akk_r = np.where(off, rnd(Akk, op_t), Akk)   # diagonal blocks solved in fp32
+                Tm = np.linalg.inv(np.eye(C) + Akk_r)
+                w = rnd(Tm @ rnd(b[:, None] * kn * np.exp(G), op_t), op_t)
+                u = rnd(Tm @ rnd(b[:, None] * vv, op_t), op_t)
+                qg = rnd(qn * np.exp(G), op_t)
+                kg = rnd(kn * np.exp(G[-1][None, :] - G), op_t)
+                Aqk = rnd(Aqk, op_t)
+                gamma = np.exp(G[-1])
+                Sr = rnd(S, op_t)
+                U = rnd(u - w @ Sr.T, op_t)
+                out[t0:t0 + L, h] = rnd(qg @ Sr.T + Aqk @ U, "bf16")[:L]
+                S = S * gamma[None, :] + U.T @ kg
+    return out
