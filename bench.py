@@ -570,7 +570,11 @@ def run_reference(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded, kda_prefill_gb300.workloads)",
         "config": {"workload": w.name, "total_tokens": w.total_tokens,
-                   "num_seqs": w.num_seqs, "heads": w.num_heads, "head_dim": 128},
+                   "num_seqs": w.num_seqs, "heads": w.num_heads, "head_dim": 128,
+                   "lower_bound": w.lower_bound,
+                   "state_pool": f"{str(w.state_pool.dtype).replace('torch.', '')} "
+                                 f"[{w.pool_storage.shape[0]},{w.num_heads},128,128]",
+                   "parallelism": "host cores of rank 0"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
                          "kind": "oracle",
                          "sample": f"each step: the whole workload ({w.total_tokens} tokens x "

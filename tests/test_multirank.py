@@ -68,4 +68,12 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1, r.stdout
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
-    assert d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["unit"] == d["unit"]
+    assert d["cpu_baseline"]["value"] == d["value"] and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["sample"]
+    # the workload keys the GPU arm reports for the same workload
+    assert d["config"]["workload"] == "tiny_varlen" and d["config"]["total_tokens"] == 96
+    assert d["config"]["lower_bound"] == -5.0
+    assert d["config"]["state_pool"] == "float32 [8,2,128,128]"
+    assert d["higher_is_better"] is True and d["unit"] == "tokens/s"
