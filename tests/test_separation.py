@@ -13,6 +13,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 # Functions of bench.py that may run the oracle: its timed CPU sample, the CPU
 # baseline and the reference arm.
 BENCH_ORACLE_FUNCS = {"_oracle_sample", "cpu_baseline", "run_reference"}
+SOURCE_DIRS = ("kda_prefill_gb300", "oracle", "tests", "include", "profiles")
 
 
 def _tracked(pattern):
@@ -20,16 +21,14 @@ def _tracked(pattern):
                          text=True)
     if out.returncode == 0 and out.stdout.strip():
         return out.stdout.split()
-    # outside a git checkout: walk the tree
+    # outside a git checkout: the source folders and the top-level files
     rx = re.compile(pattern.replace(".", r"\.").replace("*", ".*") + "$")
-    found = []
-    for d, dirs, files in os.walk(ROOT):
-        dirs[:] = [x for x in dirs if not x.startswith((".", "_work", "baseline", "gpurun_out"))]
-        for f in files:
-            rel = os.path.relpath(os.path.join(d, f), ROOT)
-            if rx.search(rel):
-                found.append(rel)
-    return found
+    found = [f for f in os.listdir(ROOT) if os.path.isfile(os.path.join(ROOT, f))]
+    for top in SOURCE_DIRS:
+        for d, dirs, files in os.walk(os.path.join(ROOT, top)):
+            dirs[:] = [x for x in dirs if not x.startswith((".", "__"))]
+            found += [os.path.relpath(os.path.join(d, f), ROOT) for f in files]
+    return [rel for rel in found if rx.search(rel)]
 
 
 def _imports(tree):
