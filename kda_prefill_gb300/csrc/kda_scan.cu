@@ -52,8 +52,8 @@ __global__ void __launch_bounds__(scan::kScanThreads, 1) kda_scan_mma(FwdParams 
 //   pass B  per segment, in parallel: the walk from S_start(s), writing the
 //           outputs and, for the last segment, the pool.
 // (ROCm/aiter PR #4741, "Optimizations Applied": the sequence-parallel split of
-// the state walk into segments composed afterwards; the composition through the
-// segment transitions is this build's.)
+// the state walk into segments composed afterwards; the page does not give the
+// composition, which follows from each chunk's affine map of the state.)
 constexpr size_t kPlane = kSegPlaneFloats;
 
 __device__ __forceinline__ float* seg_planes(const FwdParams& p, int P, int pair) {

@@ -76,7 +76,8 @@ def forward(q, k, v, g_raw, beta_raw, cu, init, flags, lb, C=64, eps=1e-6):
 # and of the incoming state; chaining S_start(s + 1) = S_start(s) Phi_s + N_s and
 # walking each segment from its start state gives the serial walk's outputs and
 # final state.  (ROCm/aiter PR #4741, "Optimizations Applied", splits the state
-# walk of long sequences into segments; this composition is the build's own.)
+# walk of long sequences into segments; the page does not give the composition,
+# which follows from each chunk's affine map of the state.)
 # ---------------------------------------------------------------------------
 
 def _padded_tiles(q, k, v, g_raw, beta_raw, lb, t_begin, t_end, h, C, eps):
