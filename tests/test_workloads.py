@@ -81,6 +81,8 @@ def test_varlen_length_draw():
     assert all(0 <= x <= 2048 for x in lens)
     n_empty = sum(1 for x in lens if x == 0)
     assert n_empty <= 20  # binomial(128, 0.05): mean 6.4
+    # the draw itself (its mean would be 128 * 0.95 * 1024.5, about 124.6K tokens)
+    assert (sum(lens), n_empty) == (113251, 8)
     # a larger draw of the same rule shows its two parts
     big = wl._varlen_lengths(torch.Generator().manual_seed(11), n=20000)
     frac_empty = sum(1 for x in big if x == 0) / len(big)
