@@ -182,7 +182,10 @@ class PinnedRing {
             }
         }
         pending_.push_back(Pending{lo, hi, nullptr});
-        cudaEventCreateWithFlags(&pending_.back().ev, cudaEventDisableTiming);
+        if (cudaEventCreateWithFlags(&pending_.back().ev, cudaEventDisableTiming) != cudaSuccess) {
+            pending_.pop_back();
+            return nullptr;
+        }
         *done = &pending_.back().ev;
         head_ = hi;
         return static_cast<char*>(base_) + lo;
@@ -287,9 +290,15 @@ class MetaCache {
             return cuda_fail(e, "cudaMallocAsync (metadata)");
         }
         e = cudaMemcpyAsync(m->dev, host, bytes, cudaMemcpyHostToDevice, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (metadata upload)");
         if (done) cudaEventRecord(*done, stream);
-        cudaEventCreateWithFlags(&m->ready, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ready, cudaEventDisableTiming);
+        if (e != cudaSuccess) {  // nothing refers to the entry yet: release it
+            cudaStreamSynchronize(stream);
+            cudaFreeAsync(m->dev, stream);
+            if (m->host_own) cudaFreeHost(m->host_own);
+            delete m;
+            return cuda_fail(e, "metadata upload");
+        }
         cudaEventRecord(m->ready, stream);
         m->upload_stream = stream;
         m->stamp = ++clock;
