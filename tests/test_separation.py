@@ -92,3 +92,21 @@ def test_nothing_tracked_refers_to_the_scratch_folder():
         if rel == "tests/test_separation.py":
             continue
         assert "_work/" not in text and "'_work'" not in text and '"_work"' not in text, rel
+
+
+def test_product_uses_no_compiler_layer():
+    """The compute path is the CUDA library: the package and the entry points
+    import no Triton and call no torch.compile."""
+    for rel in _tracked("kda_prefill_gb300/*.py") + ["__graft_entry__.py", "bench.py"]:
+        tree = _parse(rel)
+        mods = {m for m, _ in _imports(tree)}
+        assert "triton" not in mods, rel
+        for node in ast.walk(tree):
+            if isinstance(node, ast.Attribute) and node.attr == "compile":
+                assert not (isinstance(node.value, ast.Name) and node.value.id == "torch"), rel
+
+
+def test_build_targets_sm_103a_only():
+    from kda_prefill_gb300 import build as kbuild
+    assert kbuild.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert "-lineinfo" in kbuild._flags()
