@@ -271,8 +271,11 @@ KDA_API const char* kda_kernel_name(int i);
 enum kda_status_bits {
     KDA_STATUS_WAIT_TIMEOUT = 1, /* a bounded wait in a kernel gave up: results incomplete */
     KDA_STATUS_SMEM_ALIGN = 2,   /* shared memory not 1 KB aligned: the intra kernel did nothing */
-    KDA_STATUS_BAD_SLOT = 4      /* a state index outside [0, num_slots): that sequence's
+    KDA_STATUS_BAD_SLOT = 4,     /* a state index outside [0, num_slots): that sequence's
                                     slot was neither read nor written */
+    KDA_STATUS_BOUNDS_MISMATCH = 8 /* kda_chunk_fwd_noalloc only: cu_seqlens (device) and
+                                      cu_seqlens_host disagree; the call computed nothing
+                                      (out, the pool and every other buffer unchanged) */
 };
 KDA_API int kda_check_status(const void* workspace, kda_stream_t stream, int* status);
 
@@ -300,12 +303,22 @@ KDA_API int kda_set_fused_launch(int enable);
  *
  * It takes the arguments of kda_chunk_fwd without the workspace, and
  * cu_seqlens_host is required (its values size the launch; the chunk table
- * itself is built on the device from cu_seqlens).  Scratch memory comes from a
+ * itself is built on the device from cu_seqlens).  cu_seqlens and
+ * cu_seqlens_host must hold the same values.  The device copy is not trusted:
+ * the table is built from it clamped into [0, total_tokens] and made
+ * non-decreasing, with every write bounded, and its totals and a checksum are
+ * compared with the host copy's; on any difference no kernel of the call
+ * computes anything and kda_check_status(NULL, stream, &s) reports
+ * KDA_STATUS_BOUNDS_MISMATCH (the return value stays KDA_OK: the difference
+ * is found on the device, after the call has returned).  Scratch memory comes from a
  * fixed array of KDA_NOALLOC_SCRATCH_BYTES compiled into the library; every
- * GPU that loads the library holds it until process exit.  Sizes whose need,
- * kda_workspace_size(total_tokens, num_seqs, num_heads) plus the chunk table,
- * exceeds that array are rejected with KDA_ERR_WORKSPACE and a message giving
- * both numbers (64 MiB holds, e.g., a 4096-token prefill at 12 heads).
+ * GPU that loads the library holds it until process exit.  The need is the
+ * workspace for the call's exact chunk count (chunks of 64 tokens of the
+ * sequences longer than 8 tokens, counted from cu_seqlens_host; about 74 KB
+ * per chunk and head) plus the chunk table; sizes whose need exceeds the array
+ * are rejected with KDA_ERR_WORKSPACE and a message giving both numbers
+ * (64 MiB holds, e.g., a 4096-token prefill at 12 heads, or thousands of
+ * one-token decode sequences).
  *
  * The first call on a device looks up the array's device address (a CUDA
  * runtime query, no allocation), so make the first call on each device before

@@ -17,7 +17,7 @@ __all__ = [
     "chunk_fwd", "chunk_fwd_dense", "workspace_size", "chunk_size", "plan_chunks",
     "release_cache", "cache_entries", "load_library", "KDAError", "STATE_DTYPES",
     "set_kernel_timing", "kernel_times", "set_fused_launch", "check_status",
-    "STATUS_WAIT_TIMEOUT", "STATUS_SMEM_ALIGN", "STATUS_BAD_SLOT",
+    "STATUS_WAIT_TIMEOUT", "STATUS_SMEM_ALIGN", "STATUS_BAD_SLOT", "STATUS_BOUNDS_MISMATCH",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -147,6 +147,7 @@ def set_kernel_timing(enable: bool) -> None:
 STATUS_WAIT_TIMEOUT = 1
 STATUS_SMEM_ALIGN = 2
 STATUS_BAD_SLOT = 4
+STATUS_BOUNDS_MISMATCH = 8
 
 
 def check_status(workspace: Optional[torch.Tensor] = None, stream=None) -> int:

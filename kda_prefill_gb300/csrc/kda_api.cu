@@ -143,52 +143,47 @@ void meta_fill(const int32_t* cu, int32_t N, const MetaLayout& L, int32_t* buf) 
 }
 
 // ---------------------------------------------------------------------------
-// Pinned staging ring for uploads and the read-back.  Allocated once per
-// process; a region is reused only after the copy that last used it has
-// completed.
+// Pinned staging for the metadata uploads and the bounds read-back: a set of
+// pinned host blocks, each used as a ring.  A region is handed out again only
+// once the copy that last used it has completed, which is checked with
+// cudaEventQuery: acquiring never waits for the GPU.  When the region the next
+// copy needs is still in flight in every block (the GPU is behind by more than
+// a block's worth of uploads), another block is allocated and kept for later
+// calls; requests larger than a block get a block of their own size class,
+// reused in the same way.  Only past kMaxBlocks blocks does a request wait, for
+// the oldest copy of its block, so that a runaway producer cannot pin unbounded
+// host memory.
 // ---------------------------------------------------------------------------
-class PinnedRing {
+class PinnedPool {
   public:
-    static constexpr size_t kBytes = size_t(8) << 20;
+    static constexpr size_t kBlock = size_t(8) << 20;
+    static constexpr int kMaxBlocks = 32;
 
-    // Returns a staging area of `bytes` (16-aligned) or nullptr on failure.
-    // The caller records `*done` after enqueueing its copy.
-    void* acquire(size_t bytes, cudaEvent_t** done, bool* owned_separately) {
+    // Returns a staging area of `bytes` (256-aligned) or nullptr on failure.
+    // The caller records `*done` on its stream after enqueueing the copy.
+    void* acquire(size_t bytes, cudaEvent_t** done) {
         bytes = (bytes + 255) & ~size_t(255);
-        *owned_separately = false;
-        if (bytes > kBytes) {
-            void* p = nullptr;
-            if (cudaHostAlloc(&p, bytes, cudaHostAllocDefault) != cudaSuccess) return nullptr;
-            *owned_separately = true;
-            *done = nullptr;
-            return p;
+        const size_t cap = block_size(bytes);
+        for (auto& b : blocks_) {
+            if (b.cap != cap) continue;
+            void* p = try_block(b, bytes, done);
+            if (p) return p;
         }
-        if (!base_) {
-            if (cudaHostAlloc(&base_, kBytes, cudaHostAllocDefault) != cudaSuccess) {
-                base_ = nullptr;
-                return nullptr;
-            }
+        if ((int)blocks_.size() < kMaxBlocks) {
+            Block b;
+            if (cudaHostAlloc(&b.base, cap, cudaHostAllocDefault) != cudaSuccess) return nullptr;
+            b.cap = cap;
+            blocks_.push_back(std::move(b));
+            return try_block(blocks_.back(), bytes, done);
         }
-        if (head_ + bytes > kBytes) head_ = 0;
-        const size_t lo = head_, hi = head_ + bytes;
-        // wait for (and drop) earlier copies that used this region
-        for (auto it = pending_.begin(); it != pending_.end();) {
-            if (it->lo < hi && lo < it->hi) {
-                cudaEventSynchronize(it->ev);
-                cudaEventDestroy(it->ev);
-                it = pending_.erase(it);
-            } else {
-                ++it;
-            }
+        // every block of this size is busy and no more may be added: wait for
+        // the region of the first one (the only blocking case)
+        for (auto& b : blocks_) {
+            if (b.cap != cap) continue;
+            void* p = take(b, bytes, done, /*wait=*/true);
+            if (p) return p;
         }
-        pending_.push_back(Pending{lo, hi, nullptr});
-        if (cudaEventCreateWithFlags(&pending_.back().ev, cudaEventDisableTiming) != cudaSuccess) {
-            pending_.pop_back();
-            return nullptr;
-        }
-        *done = &pending_.back().ev;
-        head_ = hi;
-        return static_cast<char*>(base_) + lo;
+        return nullptr;
     }
 
   private:
@@ -196,9 +191,48 @@ class PinnedRing {
         size_t lo, hi;
         cudaEvent_t ev;
     };
-    void* base_ = nullptr;
-    size_t head_ = 0;
-    std::list<Pending> pending_;
+    struct Block {
+        void* base = nullptr;
+        size_t cap = 0, head = 0;
+        std::list<Pending> pending;
+    };
+
+    static size_t block_size(size_t bytes) {
+        size_t cap = kBlock;
+        while (cap < bytes) cap <<= 1;
+        return cap;
+    }
+
+    static void* try_block(Block& b, size_t bytes, cudaEvent_t** done) {
+        return take(b, bytes, done, /*wait=*/false);
+    }
+
+    // The region at the block's head (wrapping to the start when the tail is
+    // too short), if every earlier copy into it has completed (or, with
+    // `wait`, after waiting for them).
+    static void* take(Block& b, size_t bytes, cudaEvent_t** done, bool wait) {
+        const size_t lo = (b.head + bytes > b.cap) ? 0 : b.head, hi = lo + bytes;
+        for (auto it = b.pending.begin(); it != b.pending.end();) {
+            if (it->lo < hi && lo < it->hi) {
+                cudaError_t q = wait ? cudaEventSynchronize(it->ev) : cudaEventQuery(it->ev);
+                if (q == cudaErrorNotReady) return nullptr;
+                cudaEventDestroy(it->ev);
+                it = b.pending.erase(it);
+            } else {
+                ++it;
+            }
+        }
+        b.pending.push_back(Pending{lo, hi, nullptr});
+        if (cudaEventCreateWithFlags(&b.pending.back().ev, cudaEventDisableTiming) != cudaSuccess) {
+            b.pending.pop_back();
+            return nullptr;
+        }
+        *done = &b.pending.back().ev;
+        b.head = hi;
+        return static_cast<char*>(b.base) + lo;
+    }
+
+    std::vector<Block> blocks_;
 };
 
 struct MetaEntry {
@@ -206,7 +240,6 @@ struct MetaEntry {
     int device = 0;
     MetaLayout layout;
     int32_t* dev = nullptr;
-    void* host_own = nullptr;  // pinned buffer owned by this entry (large metadata only)
     cudaEvent_t ready = nullptr;
     cudaStream_t upload_stream = nullptr;
     bool captured = false;
@@ -220,7 +253,7 @@ class MetaCache {
 
     std::mutex mu;
     std::map<std::vector<int32_t>, MetaEntry*> map;
-    PinnedRing ring;
+    PinnedPool ring;
     uint64_t clock = 0;
 
     // Finds or builds the entry for these bounds; enqueues the upload on a miss
@@ -275,27 +308,23 @@ class MetaCache {
         m->layout = meta_layout(cu, N);
         const size_t bytes = m->layout.words * sizeof(int32_t);
         cudaEvent_t* done = nullptr;
-        bool separate = false;
-        void* host = ring.acquire(bytes, &done, &separate);
+        void* host = ring.acquire(bytes, &done);
         if (!host) {
             delete m;
             return fail(KDA_ERR_CUDA, "pinned staging allocation failed");
         }
-        if (separate) m->host_own = host;
         meta_fill(cu, N, m->layout, static_cast<int32_t*>(host));
         e = cudaMallocAsync(reinterpret_cast<void**>(&m->dev), bytes, stream);
         if (e != cudaSuccess) {
-            if (m->host_own) cudaFreeHost(m->host_own);
+            cudaEventRecord(*done, stream);  // the staging region is free again
             delete m;
             return cuda_fail(e, "cudaMallocAsync (metadata)");
         }
         e = cudaMemcpyAsync(m->dev, host, bytes, cudaMemcpyHostToDevice, stream);
-        if (done) cudaEventRecord(*done, stream);
+        cudaEventRecord(*done, stream);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&m->ready, cudaEventDisableTiming);
         if (e != cudaSuccess) {  // nothing refers to the entry yet: release it
-            cudaStreamSynchronize(stream);
             cudaFreeAsync(m->dev, stream);
-            if (m->host_own) cudaFreeHost(m->host_own);
             delete m;
             return cuda_fail(e, "metadata upload");
         }
@@ -342,7 +371,6 @@ class MetaCache {
                 leaked_.push_back(m->dev);  // other device: released by kda_release_cache
             }
             destroy_events(m);
-            if (m->host_own) leaked_host_.push_back(m->host_own);
             map.erase(victim);
             delete m;
         }
@@ -369,22 +397,18 @@ class MetaCache {
             cudaSetDevice(m->device);
             if (cudaDeviceSynchronize() != cudaSuccess) rc = KDA_ERR_CUDA;
             cudaFree(m->dev);
-            if (m->host_own) cudaFreeHost(m->host_own);
             destroy_events(m);
             delete m;
             it = map.erase(it);
         }
         for (void* p : leaked_) cudaFree(p);
         leaked_.clear();
-        for (void* p : leaked_host_) cudaFreeHost(p);
-        leaked_host_.clear();
         cudaSetDevice(cur);
         return rc;
     }
 
   private:
     std::vector<void*> leaked_;
-    std::vector<void*> leaked_host_;
 };
 
 MetaCache& cache() {
@@ -445,15 +469,13 @@ int run_forward(const void* q, const void* k, const void* v, const void* g_raw,
                         "pass cu_seqlens_host");
         readback.resize((size_t)N + 1);
         cudaEvent_t* done = nullptr;
-        bool separate = false;
-        void* host = cache().ring.acquire(readback.size() * sizeof(int32_t), &done, &separate);
+        void* host = cache().ring.acquire(readback.size() * sizeof(int32_t), &done);
         if (!host) return fail(KDA_ERR_CUDA, "pinned staging allocation failed");
         e = cudaMemcpyAsync(host, cu_dev, readback.size() * sizeof(int32_t),
                             cudaMemcpyDeviceToHost, stream);
         if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
         if (e == cudaSuccess) std::memcpy(readback.data(), host, readback.size() * sizeof(int32_t));
-        if (done) cudaEventRecord(*done, stream);
-        if (separate) cudaFreeHost(host);
+        cudaEventRecord(*done, stream);
         if (e != cudaSuccess) return cuda_fail(e, "read-back of cu_seqlens");
         cu_host = readback.data();
         int rc = check_host_bounds(cu_host, N, T);
@@ -871,28 +893,79 @@ int noalloc_scratch(void** out) {
     return KDA_OK;
 }
 
+// Checksum of a bounds array, the same on the host and on the device: the sum
+// of cu[n] (2n + 1) modulo 2^32.  Two arrays that pass the device checks below
+// but differ anywhere give different sums except in contrived cases.
+inline uint32_t bounds_sum(const int32_t* cu, int32_t N) {
+    uint32_t s = 0;
+    for (int32_t n = 0; n <= N; ++n) s += (uint32_t)cu[n] * (uint32_t)(2 * n + 1);
+    return s;
+}
+
+// What the host derived from cu_seqlens_host, for the device to compare with.
+struct HostPlan {
+    int64_t T;
+    int64_t cap_chunks;  // chunk-table capacity (entries)
+    int64_t n_chunks;
+    int32_t n_long, max_long;
+    uint32_t sum;
+};
+
 // Chunk table and sequence routing from the device bounds, one CTA: per
 // sequence its chunk count and whether it is long (short sequences, at most
 // kShortMax tokens, get no chunk and go to the token-by-token kernel), two
 // inclusive prefix sums in tiles of 1024 sequences, then each sequence's
 // chunks and its place in the long or the short list.  Same numbering as the
 // host planner (chunks follow the sequence's position in cu_seqlens).
+//
+// The device bounds are not trusted: they are first clamped into [0, T] and
+// made non-decreasing (a running maximum), so every token index the kernels
+// derive from them lies in [0, T), and every table write is bounded by the
+// table's capacity.  The totals (chunks, long sequences, longest sequence),
+// the first and last bound and the checksum are then compared with the host's;
+// on any difference the status word gets kStatusBounds and every kernel of
+// the call leaves on entry without reading the table.
 __global__ void __launch_bounds__(1024) kda_noalloc_meta(const int32_t* cu, int N, int C,
-                                                         int32_t* mcu, int32_t* off,
-                                                         int32_t* cseq, int32_t* ctok,
-                                                         int32_t* lng, int32_t* sht) {
+                                                         HostPlan hp, int32_t* mcu,
+                                                         int32_t* off, int32_t* cseq,
+                                                         int32_t* ctok, int32_t* lng,
+                                                         int32_t* sht, int* status) {
     __shared__ int32_t sbuf[1024];
     __shared__ int32_t lbuf[1024];
-    __shared__ int32_t carry, lcarry;
+    __shared__ int32_t mbuf[1024];
+    __shared__ int32_t carry, lcarry, bmax, lmax;
+    __shared__ uint32_t csum;
+    __shared__ volatile int bad;
     const int tid = threadIdx.x;
+    const int T = (int)hp.T;
     if (tid == 0) {
         carry = 0;
         lcarry = 0;
+        bmax = 0;  // running maximum of the clamped bounds before this tile
+        lmax = 0;
+        csum = 0;
+        bad = (N >= 0 && cu[0] != 0) ? 1 : 0;
     }
     __syncthreads();
     for (int base = 0; base < N; base += 1024) {
         const int n = base + tid;
-        const int len = (n < N) ? cu[n + 1] - cu[n] : 0;
+        // clamped bounds: b0 = bound n, b1 = bound n + 1, both in [0, T], then
+        // the running maximum over the array makes them non-decreasing
+        const int r1 = (n < N) ? cu[n + 1] : 0;
+        if (n < N && (r1 < 0 || r1 > T)) bad = 1;
+        mbuf[tid] = (n < N) ? min(max(r1, 0), T) : 0;
+        if (n < N) atomicAdd(&csum, (uint32_t)r1 * (uint32_t)(2 * (n + 1) + 1));
+        __syncthreads();
+        for (int o = 1; o < 1024; o <<= 1) {  // inclusive running maximum
+            const int x = (tid >= o) ? mbuf[tid - o] : 0;
+            __syncthreads();
+            mbuf[tid] = max(mbuf[tid], x);
+            __syncthreads();
+        }
+        const int b1 = max(mbuf[tid], bmax);
+        const int b0 = tid > 0 ? max(mbuf[tid - 1], bmax) : bmax;
+        const int len = (n < N) ? b1 - b0 : 0;
+        if (n < N && r1 < cu[n]) bad = 1;  // decreasing
         const int is_long = (n < N && len > kda::kShortMax) ? 1 : 0;
         const int nc = is_long ? (len + C - 1) / C : 0;
         sbuf[tid] = nc;
@@ -909,27 +982,33 @@ __global__ void __launch_bounds__(1024) kda_noalloc_meta(const int32_t* cu, int 
         const int excl = carry + sbuf[tid] - nc;
         const int lpos = lcarry + lbuf[tid] - is_long;  // long sequences before n
         if (n < N) {
-            mcu[n] = cu[n];
+            mcu[n] = b0;
             off[n] = excl;
-            for (int c = 0; c < nc; ++c) {
+            for (int c = 0; c < nc && (int64_t)excl + c < hp.cap_chunks; ++c) {
                 cseq[excl + c] = n;
-                ctok[excl + c] = cu[n] + c * C;
+                ctok[excl + c] = b0 + c * C;
             }
             if (is_long)
                 lng[lpos] = n;
             else
                 sht[n - lpos] = n;
+            if (nc > 0) atomicMax(&lmax, nc);
         }
         __syncthreads();
         if (tid == 1023) {
             carry += sbuf[1023];
             lcarry += lbuf[1023];
+            bmax = max(bmax, mbuf[1023]);
         }
         __syncthreads();
     }
     if (tid == 0) {
-        mcu[N] = cu[N];
+        mcu[N] = bmax;
         off[N] = carry;
+        const uint32_t sum = csum + (N >= 0 ? (uint32_t)cu[0] : 0u);
+        if (bad || bmax != T || carry != hp.n_chunks || lcarry != hp.n_long ||
+            lmax != hp.max_long || sum != hp.sum)
+            atomicOr(status, kda::kStatusBounds);
     }
 }
 
@@ -954,9 +1033,20 @@ extern "C" int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v
                          state_cache, state_stride0, num_slots, state_indices,
                          has_initial_state, out, state_dtype);
     if (rc != KDA_OK) return rc;
+    // The host bounds give the exact chunk count, so the scratch is laid out for
+    // it (not for kda_workspace_size's bound of total_tokens / C + num_seqs,
+    // which counts a partial chunk for every sequence, short ones included).
+    int64_t n_chunks = 0;
+    int32_t n_long = 0, max_long = 0;
+    for (int32_t n = 0; n < num_seqs; ++n) {
+        const int64_t len = (int64_t)cu_seqlens_host[n + 1] - cu_seqlens_host[n];
+        n_chunks += routed_chunks(len);
+        n_long += is_short(len) ? 0 : 1;
+        max_long = std::max<int32_t>(max_long, (int32_t)routed_chunks(len));
+    }
     // scratch layout: [workspace][cu | seq_off | chunk_seq | chunk_tok | long | short]
-    const int64_t bound = max_chunks(total_tokens, num_seqs);
-    const size_t ws_need = kda_workspace_size(total_tokens, num_seqs, num_heads);
+    const int64_t bound = std::max<int64_t>(n_chunks, 1);  // chunk-table capacity
+    const size_t ws_need = num_seqs > 0 ? kda::workspace_bytes(bound, num_heads) : 0;
     const size_t ws_part = (ws_need + 255) & ~size_t(255);
     const size_t meta_words = 2 * align4((size_t)num_seqs + 1) + 2 * align4((size_t)bound) +
                               2 * align4((size_t)num_seqs);
@@ -969,14 +1059,6 @@ extern "C" int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v
     void* scratch = nullptr;  // 256-byte aligned, and large enough by the check above
     rc = noalloc_scratch(&scratch);
     if (rc != KDA_OK) return rc;
-    int64_t n_chunks = 0;
-    int32_t n_long = 0, max_long = 0;
-    for (int32_t n = 0; n < num_seqs; ++n) {
-        const int64_t len = (int64_t)cu_seqlens_host[n + 1] - cu_seqlens_host[n];
-        n_chunks += routed_chunks(len);
-        n_long += is_short(len) ? 0 : 1;
-        max_long = std::max<int32_t>(max_long, (int32_t)routed_chunks(len));
-    }
 
     uint8_t* base = static_cast<uint8_t*>(scratch);
     int32_t* meta = reinterpret_cast<int32_t*>(base + ws_part);
@@ -991,8 +1073,11 @@ extern "C" int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v
     cudaError_t e = cudaMemsetAsync(base, 0, kda::kWsQueueOff + sizeof(int), stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (status)");
     if (num_seqs > 0) {
-        kda_noalloc_meta<<<1, 1024, 0, stream>>>(cu_seqlens, num_seqs, kChunk, mcu, off, cseq,
-                                                  ctok, lng, sht);
+        HostPlan hp{total_tokens, bound, n_chunks, n_long, max_long,
+                    bounds_sum(cu_seqlens_host, num_seqs)};
+        kda_noalloc_meta<<<1, 1024, 0, stream>>>(cu_seqlens, num_seqs, kChunk, hp, mcu, off,
+                                                  cseq, ctok, lng, sht,
+                                                  reinterpret_cast<int*>(base));
         e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "chunk table kernel launch");
     }
@@ -1031,6 +1116,7 @@ extern "C" int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v
     p.has_init = has_initial_state;
     p.st_dtype = state_dtype;
     p.num_slots = num_slots;
+    p.abort_word = p.status;  // the kernels skip a call whose device bounds disagree
     e = kda::launch_forward(p, stream, nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return KDA_OK;

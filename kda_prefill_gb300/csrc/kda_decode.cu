@@ -128,6 +128,7 @@ __host__ __device__ constexpr int dec_smem(int dtype) {
 constexpr int kDecSmemMax = dec_smem(1) > dec_smem(0) ? dec_smem(1) : dec_smem(0);
 
 __global__ void __launch_bounds__(kDecThreadsAll, 3) kda_decode(FwdParams p, long long n_items) {
+    if (call_aborted(p)) return;
     extern __shared__ __align__(128) uint8_t ring[];  // stages, then mbarriers
     __shared__ __align__(16) float s_q[D], s_k[D], s_a[D];  // q^, k^, a of the token
     __shared__ float s_red[2][4], s_beta;

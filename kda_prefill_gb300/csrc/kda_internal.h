@@ -92,7 +92,25 @@ struct FwdParams {
     // and the workspace area of the segments' fp32 state planes (nullptr: none)
     int max_long_chunks;
     float* seg;
+
+    // When set (the allocation-free entry point, whose chunk table is built on
+    // the device from device bounds), every kernel reads this status word on
+    // entry and does nothing if it carries kStatusBounds: the device bounds
+    // disagreed with the host bounds that sized the launch.
+    const int* abort_word;
 };
+
+// Status bit of a call whose device bounds disagree with its host bounds
+// (KDA_STATUS_BOUNDS_MISMATCH in kda.h).
+constexpr int kStatusBounds = 8;
+
+// True when the call's chunk table must not be used (see FwdParams::abort_word).
+// Every thread of a kernel calls it on entry and leaves when it is true, so a
+// kernel either runs in full or not at all.
+__device__ __forceinline__ bool call_aborted(const FwdParams& p) {
+    if (!p.abort_word) return false;
+    return (*reinterpret_cast<const volatile int*>(p.abort_word) & kStatusBounds) != 0;
+}
 
 // Element i of a raw gate / beta array (fp32, or bf16 when raw_bf16 is set).
 __device__ __forceinline__ float load_raw(const void* p, int raw_bf16, size_t i) {

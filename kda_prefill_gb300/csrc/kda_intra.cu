@@ -47,6 +47,7 @@ constexpr size_t kIntraSmem =
 // and the w/u recompute.  Slow but valid for any decay strength.
 __global__ void __launch_bounds__(kIntraThreads)
 kda_intra_exact(FwdParams p) {
+    if (call_aborted(p)) return;
     extern __shared__ float sm[];
     float* sQ = sm;             // [C][P] q, then q^
     float* sK = sQ + C * P;     // [C][P] k, then k^

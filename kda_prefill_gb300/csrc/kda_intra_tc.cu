@@ -669,6 +669,7 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
 template <bool RAW16>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
+    if (call_aborted(p)) return;
     extern __shared__ __align__(1024) uint8_t smem[];
     StaticClaims cl;
     intra_items<RAW16>(maps, p, smem, cl);
@@ -709,6 +710,7 @@ struct QueueClaims {
 template <bool RAW16>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_fused(const __grid_constant__ IntraMaps maps, FwdParams p, int split, int n_walks) {
+    if (call_aborted(p)) return;  // every CTA leaves: no walk waits on an item
     extern __shared__ __align__(1024) uint8_t smem[];
     QueueClaims cl{p.queue, reinterpret_cast<volatile int*>(smem + kBar + 32), split, n_walks,
                    p.n_chunks * p.H, -1};

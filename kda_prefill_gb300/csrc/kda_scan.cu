@@ -34,6 +34,7 @@ namespace {
 // One CTA per (long sequence, head, block of value rows).
 template <int NT>
 __global__ void __launch_bounds__(scan::kScanThreads, 1) kda_scan_mma(FwdParams p) {
+    if (call_aborted(p)) return;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int n = p.long_list ? p.long_list[blockIdx.x] : (int)blockIdx.x;
     scan::scan_walk<NT>(p, smem, n, (int)blockIdx.y, (int)blockIdx.z);
@@ -69,6 +70,7 @@ __device__ __forceinline__ void seg_pair(const FwdParams& p, int pair, int L, in
 
 template <bool PASS_B>
 __global__ void __launch_bounds__(scan::kScanThreads, 1) kda_scan_seg(FwdParams p, int P, int L) {
+    if (call_aborted(p)) return;
     extern __shared__ __align__(1024) uint8_t smem[];
     int u = blockIdx.x;
     const int z = u % (kD / 16);
@@ -117,6 +119,7 @@ static_assert(kCombRows == 4, "the rows of S_start are read as one float4");
 
 __global__ void __launch_bounds__(kCombThreads) kda_scan_combine(FwdParams p, int P, int L) {
     using namespace dev;
+    if (call_aborted(p)) return;
     extern __shared__ __align__(128) uint8_t csm[];
     float* phi = reinterpret_cast<float*>(csm);                        // [2][K][K]
     float* st = phi + 2 * kPlane;                                      // [K][kCombRows]: S_start^T
