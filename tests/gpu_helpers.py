@@ -73,8 +73,26 @@ def oracle_paged(w: Workload, heads=None):
     return out, fin
 
 
+def per_sequence_rel_l2(o_gpu, o_ref, f_gpu, f_ref, cu):
+    """Worst rel-L2 over the sequences of a packed batch: of each sequence's
+    output rows (sequences with tokens) and of its final state.  A global rel-L2
+    over a whole pack could hide a wrong result confined to a few short
+    sequences; this cannot."""
+    worst_o, worst_s = 0.0, 0.0
+    for n in range(len(cu) - 1):
+        a, b = int(cu[n]), int(cu[n + 1])
+        if b > a:
+            worst_o = max(worst_o, rel_l2(o_gpu[a:b], o_ref[a:b]))
+        if f_ref.size:
+            worst_s = max(worst_s, rel_l2(f_gpu[n], f_ref[n]))
+    return worst_o, worst_s
+
+
 def compare(run: DevRun, heads=None, tol=None):
-    """Compares a finished GPU run with the oracle; returns (out_err, state_err)."""
+    """Compares a finished GPU run with the oracle; returns (out_err, state_err),
+    the rel-L2 over the whole batch.  With `tol`, it also asserts that the
+    worst sequence of the batch (output rows and final state separately) is
+    within the same tolerance; both figures are printed."""
     w = run.w
     hsel = list(range(w.num_heads)) if heads is None else list(heads)
     torch.cuda.synchronize()
@@ -85,10 +103,15 @@ def compare(run: DevRun, heads=None, tol=None):
         np.zeros((0, len(hsel), 128, 128))
     eo = rel_l2(o_gpu, o_ref) if o_ref.size else 0.0
     es = rel_l2(f_gpu, f_ref) if f_ref.size else 0.0
+    wo, ws = per_sequence_rel_l2(o_gpu, o_ref, f_gpu, f_ref, w.cu_seqlens.numpy())
+    print(f"{w.name}: out rel-L2 {eo:.3e} (worst sequence {wo:.3e}), "
+          f"state rel-L2 {es:.3e} (worst sequence {ws:.3e})")
     if tol is not None:
         assert np.isfinite(o_gpu).all() and np.isfinite(f_gpu).all()
         assert eo <= tol, f"out rel-L2 {eo:.3e} > {tol}"
         assert es <= tol, f"state rel-L2 {es:.3e} > {tol}"
+        assert wo <= tol, f"worst sequence's out rel-L2 {wo:.3e} > {tol}"
+        assert ws <= tol, f"worst sequence's state rel-L2 {ws:.3e} > {tol}"
     return eo, es
 
 

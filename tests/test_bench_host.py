@@ -59,23 +59,26 @@ def test_state_bytes_of_the_mixed_batch():
 
 
 def test_traffic_record_follows_its_sources(tmp_path, monkeypatch):
-    rec = json.load(open(os.path.join(bench.ROOT, "profiles", "traffic.json")))
-    name, ent = next(iter(rec.items()))
-    srcs = ent["source"] if isinstance(ent["source"], list) else [ent["source"]]
-    # the committed record matches the committed sources
-    assert bench.load_traffic(name, ent["workload"]) == ent["dram_bytes_per_launch"]
-    assert bench.load_traffic(name, "another_workload") is None
-    # a copy of the tree where one source changed: the record no longer applies
+    """A traffic record applies only to the workload it was taken on and only
+    while the hash of its kernel sources is the one it records."""
+    import hashlib
+    srcs = ["kda_prefill_gb300/csrc/kda_intra_tc.cu", "kda_prefill_gb300/csrc/kda_scan_walk.cuh"]
     (tmp_path / "profiles").mkdir()
-    shutil.copy(os.path.join(bench.ROOT, "profiles", "traffic.json"), tmp_path / "profiles")
+    h = hashlib.sha256()
     for s in srcs:
         (tmp_path / s).parent.mkdir(parents=True, exist_ok=True)
         shutil.copy(os.path.join(bench.ROOT, s), tmp_path / s)
+        h.update(open(tmp_path / s, "rb").read())
+    rec = {"kda_fused": {"dram_bytes_per_launch": 123456, "workload": "prefill_16k",
+                         "source": srcs, "source_sha": h.hexdigest()[:16]}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.load_traffic(name, ent["workload"]) == ent["dram_bytes_per_launch"]
+    assert bench.load_traffic("kda_fused", "prefill_16k") == 123456
+    assert bench.load_traffic("kda_fused", "another_workload") is None
+    assert bench.load_traffic("kda_intra", "prefill_16k") is None
     with open(tmp_path / srcs[-1], "a") as f:
         f.write("\n// changed\n")
-    assert bench.load_traffic(name, ent["workload"]) is None
+    assert bench.load_traffic("kda_fused", "prefill_16k") is None
 
 
 class _DoneProc:
