@@ -67,6 +67,9 @@ def parse():
     ap.add_argument("--workload", default="prefill_16k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the table of the five named workloads (each timed on the GPU "
+                         "and with the oracle on the host cores)")
     ap.add_argument("--gather-arm", action="store_true",
                     help="also time the dense pipeline in-kernel paging replaces (gather, "
                          "dense forward, scatter, out copy) beside the paged call")
@@ -206,6 +209,127 @@ class Ranks:
 # ---------------------------------------------------------------------------
 # Our implementation
 # ---------------------------------------------------------------------------
+
+# The five workloads of the benchmark's configuration list, in its order; the
+# 1 x 16384 prefill is the headline (the JSON line's `value`), the others are
+# reported in its `workloads` table.
+TABLE_WORKLOADS = ("tiny_varlen", "prefill_4k", "prefill_16k", "varlen_batch", "mixed_bf16_pool")
+
+
+def step_bytes_of(w):
+    """Bytes one forward moves through HBM at most: inputs and outputs, the
+    chunk intermediates written and read back, the state."""
+    T, H, N = w.total_tokens, w.num_heads, w.num_seqs
+    return BYTES_PER_TOKHEAD * T * H + 2 * 74240 * H * (T // 64 + N) + state_bytes(w)
+
+
+def step_roofline(w, seconds, hbm, tflops):
+    """Roofline of one whole forward on workload `w` that took `seconds`."""
+    T, H = w.total_tokens, w.num_heads
+    bytes_alg = (BYTES_PER_TOKHEAD - raw_saving(w)) * T * H + state_bytes(w)
+    flops_alg = FLOP_PER_TOKHEAD * T * H
+    t_roof = max(bytes_alg / (hbm * 1e9), flops_alg / (tflops * 1e12))
+    return {"bytes_alg": bytes_alg, "flops_alg": flops_alg, "roofline_us": t_roof * 1e6,
+            "frac": t_roof / seconds, "achieved_gbs": bytes_alg / seconds / 1e9,
+            "frac_of_hbm": bytes_alg / seconds / 1e9 / hbm}
+
+
+class DeviceCall:
+    """A named workload resident on the device and its public-API call."""
+
+    def __init__(self, w, dev):
+        import torch
+        import kda_prefill_gb300 as kda
+        self.w, self.kda = w, kda
+        T, H, N = w.total_tokens, w.num_heads, w.num_seqs
+        self.q, self.k, self.v = w.q.to(dev), w.k.to(dev), w.v.to(dev)
+        self.g, self.b = w.g_raw.to(dev), w.beta_raw.to(dev)
+        self.cu = w.cu_seqlens.to(dev)
+        self.storage = w.pool_storage.to(dev)
+        S, stride0 = self.storage.shape
+        self.pool = self.storage.as_strided((S, H, 128, 128), (stride0, 128 * 128, 128, 1))
+        self.idx, self.hs = w.state_indices.to(dev), w.has_initial_state.to(dev)
+        self.out = torch.empty_like(self.v)
+        self.ws = torch.empty(max(kda.workspace_size(T, N, H), 256), dtype=torch.uint8,
+                              device=dev)
+
+    def __call__(self):
+        w = self.w
+        self.kda.chunk_fwd(self.q, self.k, self.v, self.g, self.b, self.cu,
+                           state_cache=self.pool, state_indices=self.idx,
+                           has_initial_state=self.hs, out=self.out,
+                           lower_bound=w.lower_bound, cu_seqlens_cpu=w.cu_seqlens,
+                           workspace=self.ws)
+
+
+def time_calls(fn, steps, stream, flush_buf=None):
+    """Milliseconds of `steps` calls of fn, CUDA events on the launching stream;
+    with `flush_buf` (a buffer larger than L2) each call is timed alone after
+    the buffer is rewritten, outside the events."""
+    import torch
+    torch.cuda.synchronize()
+    if flush_buf is not None:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        for a, z in ev:
+            flush_buf.zero_()
+            a.record(stream)
+            fn()
+            z.record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(z) for a, z in ev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def workload_table(dev, steps, warmup, hbm, tflops, headline=None, cpu=True):
+    """Each of the five named workloads timed through the public API (inputs
+    resident, L2 flushed between calls when a call moves less than twice the
+    L2), with its roofline and the oracle's throughput on the host cores."""
+    import torch
+    import kda_prefill_gb300 as kda
+    from kda_prefill_gb300 import workloads as wl
+    stream = torch.cuda.current_stream(dev)
+    table = {}
+    scratch = None
+    for name in TABLE_WORKLOADS:
+        w = wl.WORKLOADS[name]()
+        if headline is not None and name == headline[0]:
+            ms = headline[1]
+            kern = headline[2]
+        else:
+            call = DeviceCall(w, dev)
+            flush = step_bytes_of(w) < 2 * L2_BYTES
+            if flush and scratch is None:
+                scratch = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+            for _ in range(warmup):
+                call()
+            ms = time_calls(call, steps, stream, scratch if flush else None) / steps
+            kda.set_kernel_timing(True)
+            kda.kernel_times()
+            for _ in range(steps):
+                call()
+            torch.cuda.synchronize()
+            kt, kc = kda.kernel_times()
+            kda.set_kernel_timing(False)
+            kern = {n: t / max(kc, 1) * 1e3 for n, t in kt.items() if t > 0}
+            del call
+        row = {"us_per_call": ms * 1e3, "tokens_per_s": w.total_tokens / (ms / 1e3),
+               "total_tokens": w.total_tokens, "num_seqs": w.num_seqs, "heads": w.num_heads,
+               "kernels_us": kern,
+               "step_roofline": step_roofline(w, ms / 1e3, hbm, tflops)}
+        if cpu:
+            row["cpu_oracle"] = cpu_baseline(w, min_seconds=2.0)
+        table[name] = row
+    return table
+
+
 
 def run_ours(args, rank, world):
     import torch
@@ -483,6 +607,11 @@ def run_ours(args, rank, world):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
+    if world == 1 and not args.no_workloads:
+        kern_us = {n: t * 1e3 for n, t in kavg.items() if t > 0}
+        line["workloads"] = workload_table(
+            dev, min(args.steps, 20), max(args.warmup, 3), hbm, tf_burst,
+            headline=(args.workload, ms_step, kern_us), cpu=not args.no_cpu_baseline)
     print(json.dumps(line))
     ranks.close()
 
