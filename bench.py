@@ -75,6 +75,12 @@ def parse():
                          "dense forward, scatter, out copy) beside the paged call")
     ap.add_argument("--meta-miss", action="store_true",
                     help="also time calls whose bounds are new to the metadata cache")
+    ap.add_argument("--lower-bound", type=float, default=None,
+                    help="override the workload's lower_bound (below -5 the exact SIMT "
+                         "intra-chunk kernel runs)")
+    ap.add_argument("--no-fused", action="store_true",
+                    help="run the intra-chunk kernel and the scan as two launches instead of "
+                         "the fused launch (per-kernel timing and profiling)")
     ap.add_argument("--clock-seconds", type=float, default=1.5,
                     help="minimum span of the nvidia-smi clock sampling")
     return ap.parse_args()
@@ -340,8 +346,12 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(dev)
     ranks = Ranks(rank, world, "nccl", dev)
     kda.load_library()
+    if args.no_fused:
+        kda.set_fused_launch(False)
 
     w = wl.WORKLOADS[args.workload]()
+    if args.lower_bound is not None:
+        w.lower_bound = args.lower_bound
     T, H, N = w.total_tokens, w.num_heads, w.num_seqs
     q, k, v = w.q.to(dev), w.k.to(dev), w.v.to(dev)
     g, b = w.g_raw.to(dev), w.beta_raw.to(dev)

@@ -1,6 +1,7 @@
 // Device-side helpers shared by the KDA kernels: shared-memory tile layouts,
 // mbarrier waits with an iteration limit, TMA (bulk and tensor) copies,
-// ldmatrix and warp-level tensor-core MMA wrappers (inline PTX, sm_103a).
+// ldmatrix and warp-level tensor-core MMA wrappers, and the tcgen05 tensor-core
+// and tensor-memory wrappers (inline PTX, sm_103a).
 #pragma once
 
 #include <cuda.h>
@@ -176,6 +177,102 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
     float v;
     asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
     return v;
+}
+
+
+// ---------------------------------------------------------------------------
+// 5th-generation tensor cores (tcgen05): tensor-memory allocation, shared-
+// memory matrix descriptors, MMA issue, completion on an mbarrier, and
+// tensor-memory loads.  One CTA per SM uses these (cta_group::1).
+//
+// Shared-memory operands use the 128-byte swizzled tiles above: a 16-bit tile
+// of R rows x 128 columns is two R x 64 halves of 128-byte rows, an fp32 tile
+// four R x 32 quarters.  Read as an MMA operand such a tile is
+//   K-major (rows = M or N, columns = K): 8-row groups 1024 bytes apart (the
+//     stride byte offset); K advances inside a 128-byte row by moving the start
+//     address (the swizzle acts on absolute address bits, hence the 1 KB
+//     alignment) and to the next half/quarter by its size;
+//   MN-major (rows = K, columns = M or N): 8 K-rows per 1024 bytes (stride byte
+//     offset), the next 64 M/N columns one half further (leading byte offset).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) /* descriptor version */ |
+           (2ull << 61) /* 128-byte swizzle */;
+}
+
+// Instruction descriptor: fp32 accumulator, operand format fmt for A and B
+// (0 fp16, 1 bf16 for kind::f16; 2 for kind::tf32), majorness of A and B
+// (0 K-major, 1 MN-major), tile M x N.
+__host__ __device__ constexpr uint32_t mma_idesc(int fmt, int a_mn, int b_mn, int M, int N) {
+    return (1u << 4) | ((uint32_t)fmt << 7) | ((uint32_t)fmt << 10) | ((uint32_t)a_mn << 15) |
+           ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D (tensor memory) = A B^T (+ D when accumulate), 16-bit operands, K = 16.
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Same with tf32 operands (fp32 storage), K = 8.
+__device__ __forceinline__ void mma_tf32_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives on the mbarrier once every MMA this thread issued before has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Tensor-memory allocation by one whole warp; the address lands in *slot.
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's lane (32x32b shape: a warp
+// reads the 32 lanes of its quarter, warp % 4).  Complete after tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 }  // namespace dev

@@ -78,11 +78,21 @@ constexpr int kSc = 221184;    // beta[64] | NS [16][16] | F1 [4][128] | HT [4][
 constexpr int kMid = kSc + 256 + 1024 + 2048 + 4096;  // E_1, E_2 fp16 [2][128]
 constexpr int kBar = kMid + 512;
 constexpr int kSmemBytes = kBar + 64;
+// the fused launch runs scan walks in the same shared memory
+static_assert(scan::ScanSmem<2>::kTotal <= kSmemBytes, "a walk fits in the intra kernel's shared memory");
 // Reuse of the k^/P area after the tile MMAs:
 constexpr int kAqkStage = kRd32;          // A_qk fp16 [64][64] tile, to store (8 KB)
 constexpr int kNAk = kRd32 + 8192;        // -A_kk off-diagonal blocks, fp16 [64][64] (8 KB)
 constexpr int kAkd = kRd32 + 16384;       // A_kk diagonal blocks, fp32 [4][16][16] (4 KB)
-constexpr int kT16 = kRd32 + 20480;       // T_II diagonal blocks, fp16 [64][64] tile (8 KB)
+constexpr int kT16 = kRd32 + 20480;       // T = (I + A_kk)^{-1}, fp16 [64][64] tile (8 KB)
+// After the tile MMAs the k^ E_B / P area holds X = b k^ e^G (fp16 [64][128]).
+constexpr int kX = kRO;
+
+// Tensor memory of the w / u product: [w | u] = T [X | Y], an M = 64 product
+// with fp32 accumulators: chunk rows 16 q .. 16 q + 15 sit in lanes 0..15 of
+// lane quarter q (lanes 32 q ..), columns 0..127 w, 128..255 u.
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kIdescWU = mma_idesc(0, 0, 1, 64, 128);  // fp16; A K-major, B MN-major
 
 struct IntraMaps {
     CUtensorMap q, k, v, g;
@@ -134,6 +144,66 @@ __device__ __forceinline__ void pair_of(int pi, int& I, int& J) {
     J = pi - I * (I - 1) / 2;
 }
 
+// Block column J of T = (I + A_kk)^{-1} below the diagonal, by one warp:
+// T_IJ = T_II sum_{J<=m<I} (-A_Im) T_mJ for I = J+1..3, formed in transposed
+// form (T_IJ^T = (sum_m T_mJ^T (-A_Im)^T) T_II^T) so that each result is
+// already the A fragment of the next product; the warp also zeroes the blocks
+// above the diagonal in row J.  Reads -A_kk (off-diagonal, fp16) and the T_II
+// diagonal blocks from their tiles, writes T_IJ into the T tile.  Every operand
+// fragment is loaded first and the products that need only T_JJ come before the
+// dependent chain T_{J+1,J} -> T_{J+2,J} -> T_{J+3,J}.
+template <int J>
+__device__ __forceinline__ void t_column(uint8_t* smem, int lane) {
+    const int mi = lane >> 3, rr = lane & 7;
+    const uint32_t nak = smem_u32(smem + kNAk), t16 = smem_u32(smem + kT16);
+    uint32_t tf[4][4];  // T_mJ^T as fp16 A fragments, m = J..3
+    ldsm_x4_t(t16 + sw64_off(16 * J + 8 * (mi >> 1) + rr, 16 * J + 8 * (mi & 1)), tf[J][0], tf[J][1],
+              tf[J][2], tf[J][3]);
+    uint32_t nb[4][4][4];  // (-A_Im)^T B fragments, [I][m]
+    uint32_t tb[4][4];     // T_II^T B fragments
+#pragma unroll
+    for (int I = J + 1; I < 4; ++I) {
+#pragma unroll
+        for (int m = J; m < I; ++m)
+            ldsm_x4(nak + sw64_off(16 * I + 8 * (mi >> 1) + rr, 16 * m + 8 * (mi & 1)), nb[I][m][0],
+                    nb[I][m][1], nb[I][m][2], nb[I][m][3]);
+        ldsm_x4(t16 + sw64_off(16 * I + 8 * (mi >> 1) + rr, 16 * I + 8 * (mi & 1)), tb[I][0], tb[I][1],
+                tb[I][2], tb[I][3]);
+    }
+    float acc[4][2][4];
+#pragma unroll
+    for (int I = J + 1; I < 4; ++I) {  // the terms with T_JJ (m = J)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[I][nt][e] = 0.f;
+        mma_f16(acc[I][0], tf[J], nb[I][J][0], nb[I][J][1]);
+        mma_f16(acc[I][1], tf[J], nb[I][J][2], nb[I][J][3]);
+    }
+#pragma unroll
+    for (int I = J + 1; I < 4; ++I) {
+        const uint32_t ra[4] = {pack_half2(acc[I][0][0], acc[I][0][1]), pack_half2(acc[I][0][2], acc[I][0][3]),
+                                pack_half2(acc[I][1][0], acc[I][1][1]), pack_half2(acc[I][1][2], acc[I][1][3])};
+        float tv[2][4] = {};
+        mma_f16(tv[0], ra, tb[I][0], tb[I][1]);
+        mma_f16(tv[1], ra, tb[I][2], tb[I][3]);
+        tf[I][0] = pack_half2(tv[0][0], tv[0][1]);
+        tf[I][1] = pack_half2(tv[0][2], tv[0][3]);
+        tf[I][2] = pack_half2(tv[1][0], tv[1][1]);
+        tf[I][3] = pack_half2(tv[1][2], tv[1][3]);
+#pragma unroll
+        for (int I2 = I + 1; I2 < 4; ++I2) {  // T_IJ's term in the later blocks
+            mma_f16(acc[I2][0], tf[I], nb[I2][I][0], nb[I2][I][1]);
+            mma_f16(acc[I2][1], tf[I], nb[I2][I][2], nb[I2][I][3]);
+        }
+        stsm_x4_t(t16 + sw64_off(16 * I + 8 * (mi >> 1) + rr, 16 * J + 8 * (mi & 1)), tf[I][0], tf[I][1],
+                  tf[I][2], tf[I][3]);
+        // block (J, I) above the diagonal is zero
+        *reinterpret_cast<uint4*>(smem + kT16 + sw64_off(16 * J + (lane >> 1), 16 * I + 8 * (lane & 1))) =
+            make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
 // The intra-chunk items of one CTA, in the order `cl` hands them out (all
 // threads call cl.first() once and, per item, cl.claim() before and cl.next()
 // after a CTA barrier).  RAW16: raw gate and beta in bf16 (the gate tile then
@@ -146,7 +216,8 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
     float* F1 = NS + 256;   // [4][128] decay of the blocks before B (e^G at the block start)
     float* HT = F1 + 512;   // [4][2][128] decay product of each 8-row half block
     __half* MIDh = reinterpret_cast<__half*>(smem + kMid);     // [2][128] E_1, E_2 in fp16
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBar);  // [0] q,k,g  [1] v
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBar);  // [0] q,k,g  [1] v  [2] w/u MMA
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kBar + 24);  // tensor-memory base
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -163,13 +234,18 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
     if (tid == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
+        mbar_init(&bar[2], 1);
         fence_mbar_init();
         prefetch_tmap(&maps.q);
         prefetch_tmap(&maps.k);
         prefetch_tmap(&maps.v);
         prefetch_tmap(&maps.g);
     }
+    if (warp == 0) tmem_alloc(tslot, kTmemCols);
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
 
     // TMA issue (one thread).
     auto issue_inputs = [&](int it, int t0) {
@@ -573,82 +649,89 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
             bulk_commit();
         }
 
-        // ---- w = (I + A_kk)^{-1} X and u = (I + A_kk)^{-1} Y by blocked forward
-        //      substitution, in transposed form so that every operand between
-        //      steps stays in registers: warp w owns 16 of the 256 columns of
-        //      [X | Y] and forms, for I = 0..3,
-        //        R_I^T = X_I^T - sum_{J<I} W_J^T A_IJ^T,   W_I^T = R_I^T T_II^T
-        //      with the columns as the MMA rows.  An m16n8k16 accumulator holding
-        //      (column, row pair) is exactly the A fragment of the next product,
-        //      so R_I^T and the W_J^T feed the MMAs directly.  X = b k^ e^G enters
-        //      in fp32, formed per element from k^ P (still in its tile), b and the
-        //      block prefix F1; Y = b v enters as Y_I^T times the identity.  W goes
-        //      out through stmatrix.trans into the staging tiles (w in the LQ area,
-        //      u in the q^P area).
+        // ---- T = (I + A_kk)^{-1} in full: warp J forms block column J below the
+        //      diagonal, T_IJ = T_II sum_{J<=m<I} (-A_Im) T_mJ for I = J+1..3, in
+        //      transposed form (T_IJ^T = (sum T_mJ^T (-A_Im)^T) T_II^T) so that
+        //      each result is already the A fragment of the next product, and
+        //      zeroes the blocks above the diagonal in row J (t_column).
+        if (warp == 0) t_column<0>(smem, lane);
+        if (warp == 1) t_column<1>(smem, lane);
+        if (warp == 2) t_column<2>(smem, lane);
+        // ---- meanwhile the other warps form X = b k^ e^G in fp16 for the w
+        //      product (k^ P from its fp32 tile times b and the prefix F1 of the
+        //      row's block) in the free k^ E_B / P area: 16-byte pieces, 64 rows x 16
+        for (int pc = tid - 96; pc >= 0 && pc < 1024; pc += kThreads - 96) {
+            const int r = pc >> 4, c8 = (pc & 15) * 8;
+            const float br = beta[r];
+            const float* f1 = F1 + (r >> 4) * 128 + c8;
+            uint32_t w4[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const float2 kp = *reinterpret_cast<const float2*>(smem + kLk32 + sw128f_off(r, c8 + 2 * x, 64));
+                w4[x] = pack_half2(br * f1[2 * x] * kp.x, br * f1[2 * x + 1] * kp.y);
+            }
+            *reinterpret_cast<uint4*>(smem + kX + sw128_off(r, c8, 64)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+        fence_proxy_async();  // T, X and Y are read by the tensor cores
+        __syncthreads();
+
+        // ---- [w | u] = T [X | Y] on the tensor cores: A = T (K-major), B = X and
+        //      Y read MN-major from their row-major tiles (K = the chunk's rows)
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t sb = smem_u32(smem);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {  // K = 16 rows per MMA
+                const uint64_t a = sw128_desc(sb + kT16 + ks * 32, 16, 1024);
+                mma_f16_ss(tmem, a, sw128_desc(sb + kX + ks * 2048, 8192, 1024), kIdescWU, ks > 0);
+                mma_f16_ss(tmem + 128, a, sw128_desc(sb + kV + ks * 2048, 8192, 1024), kIdescWU, ks > 0);
+            }
+            mma_commit(&bar[2]);
+        }
+        const bool ok_wu = !__syncthreads_or(!mbar_wait(&bar[2], n_local & 1));
+        tc_fence_after();
+        if (!ok_wu) {  // the product never completed: report and stop (uniform)
+            if (tid == 0 && p.status) atomicOr(p.status, 1);
+            break;
+        }
+
+        // ---- w and u out of tensor memory into their staging tiles: warp w reads
+        //      lane quarter qd = w % 4, whose lanes 0..15 hold chunk rows 16 qd +
+        //      lane; part w / 4 takes 64 of the 256 columns (0, 1: w; 2, 3: u).
         {
-            const bool isu = warp >= 8;
-            const int n0 = 16 * (warp & 7);
-            const uint32_t xb = smem_u32(smem + (isu ? kV : kLQ));
-            const uint32_t nak = smem_u32(smem + kNAk), t16 = smem_u32(smem + kT16);
-            const uint32_t ub = smem_u32(smem + kLq32 + (warp & 7) * kWsUSliceBytes);  // [64][16]
-            // identity B fragments: b0 of n-tile 0 and b1 of n-tile 1 hold ones
-            // where row 2tq or 2tq + 1 equals column g
-            const uint32_t id = ((2 * tq == g8) ? 0x3c00u : 0u) | ((2 * tq + 1 == g8) ? 0x3c000000u : 0u);
-            uint32_t wf[4][4];  // W_J^T as fp16 A fragments
+            const int qd = warp & 3, part = warp >> 2;
+            const int i = 16 * qd + (lane & 15);
+            const uint32_t tcol = tmem + ((uint32_t)(32 * qd) << 16) + 64 * part;
 #pragma unroll
-            for (int I = 0; I < 4; ++I) {
-                float acc[2][4] = {};
-                if (isu) {
-                    uint32_t xa[4];
-                    ldsm_x4_t(xb + sw128_off(16 * I + 8 * (mi >> 1) + rr, n0 + 8 * (mi & 1), 64), xa[0],
-                              xa[1], xa[2], xa[3]);
-                    mma_f16(acc[0], xa, id, 0u);
-                    mma_f16(acc[1], xa, 0u, id);
-                } else {
-                    // accumulator element (column n0 + g + 8(e >> 1), row 16I + 8nt + 2tq + (e & 1))
-                    const float f1a = F1[I * 128 + n0 + g8], f1b = F1[I * 128 + n0 + g8 + 8];
+            for (int h = 0; h < 2; ++h) {
+                float x[2][16];
+                tmem_ld16(tcol + 32 * h, x[0]);
+                tmem_ld16(tcol + 32 * h + 16, x[1]);
+                tmem_wait_ld();
+                if (lane < 16) {
 #pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int row = 16 * I + 8 * nt + 2 * tq + (e & 1);
-                            const int col = n0 + g8 + 8 * (e >> 1);
-                            acc[nt][e] = beta[row] * ((e >> 1) ? f1b : f1a) *
-                                         *reinterpret_cast<const float*>(smem + kLk32 +
-                                                                         sw128f_off(row, col, 64));
+                    for (int g2 = 0; g2 < 2; ++g2) {
+                        const float* xv = x[g2];
+                        const uint4 lo = make_uint4(pack_half2(xv[0], xv[1]), pack_half2(xv[2], xv[3]),
+                                                    pack_half2(xv[4], xv[5]), pack_half2(xv[6], xv[7]));
+                        const uint4 hi = make_uint4(pack_half2(xv[8], xv[9]), pack_half2(xv[10], xv[11]),
+                                                    pack_half2(xv[12], xv[13]), pack_half2(xv[14], xv[15]));
+                        const int c16 = 32 * h + 16 * g2;  // column within the part
+                        if (part < 2) {
+                            const int c = 64 * part + c16;
+                            *reinterpret_cast<uint4*>(smem + kLQ + sw128_off(i, c, 64)) = lo;
+                            *reinterpret_cast<uint4*>(smem + kLQ + sw128_off(i, c + 8, 64)) = hi;
+                        } else {
+                            const int slice = 4 * (part - 2) + (c16 >> 4);  // 16 value columns each
+                            uint8_t* dst = smem + kLq32 + slice * kWsUSliceBytes + i * 32;
+                            *reinterpret_cast<uint4*>(dst) = lo;
+                            *reinterpret_cast<uint4*>(dst + 16) = hi;
                         }
+                    }
                 }
-#pragma unroll
-                for (int J = 0; J < I; ++J) {
-                    uint32_t b4[4];
-                    ldsm_x4(nak + sw64_off(16 * I + 8 * (mi >> 1) + rr, 16 * J + 8 * (mi & 1)), b4[0], b4[1],
-                            b4[2], b4[3]);
-                    mma_f16(acc[0], wf[J], b4[0], b4[1]);
-                    mma_f16(acc[1], wf[J], b4[2], b4[3]);
-                }
-                const uint32_t ra[4] = {pack_half2(acc[0][0], acc[0][1]), pack_half2(acc[0][2], acc[0][3]),
-                                        pack_half2(acc[1][0], acc[1][1]), pack_half2(acc[1][2], acc[1][3])};
-                float wv[2][4] = {};
-                {
-                    uint32_t b4[4];
-                    ldsm_x4(t16 + sw64_off(16 * I + 8 * (mi >> 1) + rr, 16 * I + 8 * (mi & 1)), b4[0], b4[1],
-                            b4[2], b4[3]);
-                    mma_f16(wv[0], ra, b4[0], b4[1]);
-                    mma_f16(wv[1], ra, b4[2], b4[3]);
-                }
-                wf[I][0] = pack_half2(wv[0][0], wv[0][1]);
-                wf[I][1] = pack_half2(wv[0][2], wv[0][3]);
-                wf[I][2] = pack_half2(wv[1][0], wv[1][1]);
-                wf[I][3] = pack_half2(wv[1][2], wv[1][3]);
-                __syncwarp();  // Y_I of these columns is read: W_I may overwrite it
-                const int row = 16 * I + 8 * (mi >> 1) + rr;
-                if (isu)
-                    stsm_x4_t(ub + row * 32 + 16 * (mi & 1), wf[I][0], wf[I][1], wf[I][2], wf[I][3]);
-                else
-                    stsm_x4_t(xb + sw128_off(row, n0 + 8 * (mi & 1), 64), wf[I][0], wf[I][1], wf[I][2],
-                              wf[I][3]);
             }
         }
+        tc_fence_before();
         fence_proxy_async();
         __syncthreads();
         if (tid == 0) {
@@ -664,6 +747,11 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
         bulk_wait_all();  // stores complete before the CTA releases its smem
         if (p.ready && prev >= 0) publish_ready(p.ready + prev);
     }
+    // every tensor-memory read has completed (tcgen05.wait::ld) before the release
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 template <bool RAW16>

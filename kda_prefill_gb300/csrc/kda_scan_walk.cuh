@@ -51,6 +51,10 @@ constexpr int round1k(int x) { return (x + 1023) / 1024 * 1024; }
 
 constexpr int kStages = 3;    // chunk intermediates in flight per CTA
 constexpr int kPrefetch = 6;  // chunks ahead of the stage loads asked of L2
+// Slots of the S and U rings shared by the state and output warps: with two,
+// the state warps may run one chunk ahead of the output warps (three measured
+// slower: 188 against 183 us for the 16K prefill's scan).
+constexpr int kRing = 2;
 
 template <int NT>
 struct ScanSmem {
@@ -59,13 +63,14 @@ struct ScanSmem {
     static constexpr int kSharedPad = round1k(kShared);
     static constexpr int kU = (VS / 16) * kWsUSliceBytes;    // the CTA's u columns
     static constexpr int kStage = kSharedPad + round1k(kU);
-    static constexpr int kS16 = kStages * kStage;            // 2 slots x [VS][128] fp16
+    static constexpr int kS16 = kStages * kStage;            // kRing slots x [VS][128] fp16
     static constexpr int kS16Slot = VS * 256;
-    static constexpr int kUt = kS16 + 2 * kS16Slot;          // 2 slots x [VS][64] fp16
+    static constexpr int kUt = kS16 + kRing * kS16Slot;      // kRing slots x [VS][64] fp16
     static constexpr int kUtSlot = VS * 128;
-    static constexpr int kBar = kUt + 2 * kUtSlot;           // mbarriers
-    static constexpr int kAbort = kBar + 96;                 // int: a state warp gave up
+    static constexpr int kBar = kUt + kRing * kUtSlot;       // mbarriers (2 kStages + 2 kRing)
+    static constexpr int kAbort = kBar + 8 * (2 * kStages + 2 * kRing);  // int: a state warp gave up
     static constexpr int kTotal = kBar + 128;
+    static_assert(kAbort + 4 <= kTotal, "mbarriers and the abort flag fit");
 };
 
 constexpr int kStateWarps = 4, kOutWarps = 4;
@@ -115,8 +120,8 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
     constexpr int VS = L::VS;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);  // [kStages]
     uint64_t* empty = full + kStages;                               // [kStages]
-    uint64_t* sready = full + 2 * kStages;                          // [2]
-    uint64_t* sfree = sready + 2;                                   // [2]
+    uint64_t* sready = full + 2 * kStages;                          // [kRing]
+    uint64_t* sfree = sready + kRing;                               // [kRing]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
 
     const int v0 = z * VS;  // first value row of this CTA
@@ -141,10 +146,10 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kStateWarps + kOutWarps);
         }
-        mbar_init(&sready[0], 1);
-        mbar_init(&sready[1], 1);
-        mbar_init(&sfree[0], kOutWarps);
-        mbar_init(&sfree[1], kOutWarps);
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(&sready[i], 1);
+            mbar_init(&sfree[i], kOutWarps);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -202,8 +207,8 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
     if (warp >= kStateWarps) {
         const int wr = warp - kStateWarps;  // chunk rows 16wr..16wr+15
         for (int lc = 0; lc < nch; ++lc) {
-            const int b = lc & 1, sg = lc % kStages;
-            const uint32_t par = (lc >> 1) & 1;
+            const int b = lc % kRing, sg = lc % kStages;
+            const uint32_t par = (lc / kRing) & 1;
             if (!mbar_wait(&full[sg], (lc / kStages) & 1) || !mbar_wait(&sready[b], par)) {
                 if (p.status) atomicOr(p.status, 1);
                 break;
@@ -345,7 +350,7 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
 
     bool failed = false;
     for (int lc = 0; lc < nch; ++lc) {
-        const int b = lc & 1, sg = lc % kStages;
+        const int b = lc % kRing, sg = lc % kStages;
         const bool ok = mbar_wait(&full[sg], (lc / kStages) & 1);  // voted below, before any write
         const uint32_t st = stage_base(sg);
         const uint32_t tw = st + kWsWOff, tkg = st + kWsKGOff;
@@ -388,6 +393,15 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
             stsm_x4_t(ut + sw64_off(vrow, ccol), uf[2 * np][0], uf[2 * np][1], uf[2 * np + 1][0],
                       uf[2 * np + 1][1]);
         }
+        // kg^T fragments of the update, loaded before the barrier (they do not
+        // depend on U) so that their latency overlaps the wait
+        uint32_t kga[4][2][4];
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+                ldsm_x4_t(tkg + sw128_off(16 * ks + rr + 8 * (mi >> 1), 32 * wr + 16 * mt + 8 * (mi & 1), 64),
+                          kga[ks][mt][0], kga[ks][mt][1], kga[ks][mt][2], kga[ks][mt][3]);
         const int abort1 = state_sync_flag(!ok);  // a copy never landed (tested below)
         if (tid == 0) mbar_arrive(&sready[b]);  // S (published last step) and U of this chunk
 
@@ -401,14 +415,9 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
                 ldsm_x4(ut + sw64_off(16 * np + rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1)),
                         bb[2 * np][0], bb[2 * np][1], bb[2 * np + 1][0], bb[2 * np + 1][1]);
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                uint32_t a[4];
-                ldsm_x4_t(tkg + sw128_off(16 * ks + rr + 8 * (mi >> 1),
-                                          32 * wr + 16 * mt + 8 * (mi & 1), 64),
-                          a[0], a[1], a[2], a[3]);
+            for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma_f16(accS[mt][nt], a, bb[nt][0], bb[nt][1]);
-            }
+                for (int nt = 0; nt < NT; ++nt) mma_f16(accS[mt][nt], kga[ks][mt], bb[nt][0], bb[nt][1]);
         }
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
@@ -429,11 +438,12 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[sg]);  // w, kg, gamma and u of this stage are read
 
-        // publish the next chunk's incoming S in the other slot once the output
-        // warps are done with the chunk that used it
-        const int nb = b ^ 1;
+        // publish the next chunk's incoming S in the next slot once the output
+        // warps are done with the chunk that used it (kRing - 1 chunks back;
+        // that also frees the slot the next chunk's U goes to)
+        const int nb = (lc + 1) % kRing;
         bool ok2 = true;
-        if (lc >= 1) ok2 = mbar_wait(&sfree[nb], ((lc - 1) >> 1) & 1);
+        if (lc >= kRing - 1) ok2 = mbar_wait(&sfree[nb], ((lc + 1 - kRing) / kRing) & 1);
         if (ok2) write_s16(nb);
         const int abort2 = state_sync_flag(!ok2);
         load_sfrag(nb);
