@@ -642,6 +642,25 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
                 put(1, tI, tJ, acc[1]);
             }
         }
+        // ---- X = b k^ e^G in fp16 for the w product, by the 12 warps that do not
+        //      invert (beside the 16x16 inverses): k^ P from its fp32 tile (a lane
+        //      reads one 16-byte chunk, four columns, a warp two whole rows, so a
+        //      read takes the four wavefronts 512 bytes need) times b and the
+        //      prefix F1 of the row's block, into the free k^ E_B / P area
+        if (!(warp < 8 && (warp & 1))) {
+            const int xw = warp < 8 ? (warp >> 1) : warp - 4;  // 0..11
+            for (int pc = 32 * xw + lane; pc < 2048; pc += 12 * 32) {
+                const int r = pc >> 5, qt = (pc >> 3) & 3, cc = pc & 7;
+                const int c = 32 * qt + 4 * cc;
+                const float4 kp = *reinterpret_cast<const float4*>(
+                    smem + kLk32 + qt * 8192 + r * 128 + ((cc ^ (r & 7)) << 4));
+                const float4 f1 = *reinterpret_cast<const float4*>(F1 + (r >> 4) * 128 + c);
+                const float br = beta[r];
+                *reinterpret_cast<uint2*>(smem + kX + sw128_off(r, c, 64)) =
+                    make_uint2(pack_half2(br * f1.x * kp.x, br * f1.y * kp.y),
+                               pack_half2(br * f1.z * kp.z, br * f1.w * kp.w));
+            }
+        }
         fence_proxy_async();  // the A_qk staging tile is read by the bulk store
         __syncthreads();
         if (tid == 0) {
@@ -657,22 +676,6 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
         if (warp == 0) t_column<0>(smem, lane);
         if (warp == 1) t_column<1>(smem, lane);
         if (warp == 2) t_column<2>(smem, lane);
-        // ---- meanwhile the other warps form X = b k^ e^G in fp16 for the w
-        //      product (k^ P from its fp32 tile times b and the prefix F1 of the
-        //      row's block) in the free k^ E_B / P area: 16-byte pieces, 64 rows x 16
-        for (int pc = tid - 96; pc >= 0 && pc < 1024; pc += kThreads - 96) {
-            const int r = pc >> 4, c8 = (pc & 15) * 8;
-            const float br = beta[r];
-            const float* f1 = F1 + (r >> 4) * 128 + c8;
-            uint32_t w4[4];
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-                const float2 kp = *reinterpret_cast<const float2*>(smem + kLk32 + sw128f_off(r, c8 + 2 * x, 64));
-                w4[x] = pack_half2(br * f1[2 * x] * kp.x, br * f1[2 * x + 1] * kp.y);
-            }
-            *reinterpret_cast<uint4*>(smem + kX + sw128_off(r, c8, 64)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-        }
-        fence_proxy_async();  // T, X and Y are read by the tensor cores
         __syncthreads();
 
         // ---- [w | u] = T [X | Y] on the tensor cores: A = T (K-major), B = X and
@@ -702,16 +705,16 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
             const int qd = warp & 3, part = warp >> 2;
             const int i = 16 * qd + (lane & 15);
             const uint32_t tcol = tmem + ((uint32_t)(32 * qd) << 16) + 64 * part;
+            float x[4][16];  // the part's 64 columns, loaded before one wait
+#pragma unroll
+            for (int h = 0; h < 4; ++h) tmem_ld16(tcol + 16 * h, x[h]);
+            tmem_wait_ld();
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                float x[2][16];
-                tmem_ld16(tcol + 32 * h, x[0]);
-                tmem_ld16(tcol + 32 * h + 16, x[1]);
-                tmem_wait_ld();
                 if (lane < 16) {
 #pragma unroll
                     for (int g2 = 0; g2 < 2; ++g2) {
-                        const float* xv = x[g2];
+                        const float* xv = x[2 * h + g2];
                         const uint4 lo = make_uint4(pack_half2(xv[0], xv[1]), pack_half2(xv[2], xv[3]),
                                                     pack_half2(xv[4], xv[5]), pack_half2(xv[6], xv[7]));
                         const uint4 hi = make_uint4(pack_half2(xv[8], xv[9]), pack_half2(xv[10], xv[11]),
