@@ -140,6 +140,11 @@ void meta_fill(const int32_t* cu, int32_t N, const MetaLayout& L, int32_t* buf) 
     }
     mcu[N] = cu[N];
     off[N] = (int32_t)j;
+    // longest first: the scan launches its walks in this order, so that the long
+    // walks start in the first wave and the short ones fill the last
+    std::stable_sort(lng, lng + nl, [&](int32_t a, int32_t b) {
+        return cu[a + 1] - cu[a] > cu[b + 1] - cu[b];
+    });
 }
 
 // ---------------------------------------------------------------------------

@@ -673,9 +673,12 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
         //      transposed form (T_IJ^T = (sum T_mJ^T (-A_Im)^T) T_II^T) so that
         //      each result is already the A fragment of the next product, and
         //      zeroes the blocks above the diagonal in row J (t_column).
-        if (warp == 0) t_column<0>(smem, lane);
-        if (warp == 1) t_column<1>(smem, lane);
-        if (warp == 2) t_column<2>(smem, lane);
+        if (warp < 3) {
+            if (warp == 0) t_column<0>(smem, lane);
+            if (warp == 1) t_column<1>(smem, lane);
+            if (warp == 2) t_column<2>(smem, lane);
+            fence_proxy_async();  // T's blocks (generic stores) are read by the tensor cores
+        }
         __syncthreads();
 
         // ---- [w | u] = T [X | Y] on the tensor cores: A = T (K-major), B = X and

@@ -31,13 +31,18 @@
 namespace kda {
 namespace {
 
-// One CTA per (long sequence, head, block of value rows).
+// One CTA per (long sequence, head, block of value rows), the sequence the
+// slowest-varying index: CTAs start in launch order, so the walks of the list's
+// first sequences (the host orders it longest first) start in the first wave.
 template <int NT>
 __global__ void __launch_bounds__(scan::kScanThreads, 1) kda_scan_mma(FwdParams p) {
     if (call_aborted(p)) return;
     extern __shared__ __align__(1024) uint8_t smem[];
-    const int n = p.long_list ? p.long_list[blockIdx.x] : (int)blockIdx.x;
-    scan::scan_walk<NT>(p, smem, n, (int)blockIdx.y, (int)blockIdx.z);
+    constexpr int kGroups = kD / scan::ScanSmem<NT>::VS;
+    const int b = (int)blockIdx.x;
+    const int z = b % kGroups, h = (b / kGroups) % p.H, sq = b / (kGroups * p.H);
+    const int n = p.long_list ? p.long_list[sq] : sq;
+    scan::scan_walk<NT>(p, smem, n, h, z);
 }
 
 // ---- segmented scan --------------------------------------------------------
@@ -238,8 +243,8 @@ cudaError_t launch_scan_nt(const FwdParams& p, cudaStream_t s) {
     }
     const int n_seq = p.long_list ? p.n_long : p.N;
     if (n_seq <= 0) return cudaSuccess;
-    dim3 grid((unsigned)n_seq, (unsigned)p.H, (unsigned)(kD / L::VS));
-    kda_scan_mma<NT><<<grid, scan::kScanThreads, L::kTotal, s>>>(p);
+    const long blocks = (long)n_seq * p.H * (kD / L::VS);
+    kda_scan_mma<NT><<<(unsigned)blocks, scan::kScanThreads, L::kTotal, s>>>(p);
     return cudaGetLastError();
 }
 
