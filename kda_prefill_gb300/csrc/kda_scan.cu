@@ -252,9 +252,11 @@ cudaError_t launch_scan_nt(const FwdParams& p, cudaStream_t s) {
 
 int scan_groups(int N, int H, int num_sms) {
     // 16 value rows per CTA while (sequence, head) pairs are few enough for the
-    // finer split to fill the GPU, 32 otherwise.
+    // finer split to fill the GPU, else 64: the head-wide chunk operands each CTA
+    // reads then serve four times as many value rows (measured against 32 rows
+    // per CTA: mixed batch 70.3 against 76.6 us, varlen batch 620 against 699 us).
     const long pairs = (long)N * H;
-    return pairs * 8 <= 2L * num_sms ? 1 : 2;
+    return pairs * 8 <= 2L * num_sms ? 1 : 4;
 }
 
 int scan_segments(const FwdParams& p, int num_sms, int* L) {
@@ -277,7 +279,7 @@ cudaError_t launch_scan(const FwdParams& p, int groups, cudaStream_t s) {
     int L = 0;
     const int P = scan_segments(p, num_sms(), &L);
     if (P > 0) return launch_scan_segmented(p, P, L, s);
-    return groups <= 1 ? launch_scan_nt<2>(p, s) : launch_scan_nt<4>(p, s);
+    return groups <= 1 ? launch_scan_nt<2>(p, s) : launch_scan_nt<8>(p, s);
 }
 
 }  // namespace kda

@@ -49,7 +49,6 @@ constexpr int D = kD;
 
 constexpr int round1k(int x) { return (x + 1023) / 1024 * 1024; }
 
-constexpr int kStages = 3;    // chunk intermediates in flight per CTA
 constexpr int kPrefetch = 6;  // chunks ahead of the stage loads asked of L2
 // Slots of the S and U rings shared by the state and output warps: with two,
 // the state warps may run one chunk ahead of the output warps (three measured
@@ -59,6 +58,9 @@ constexpr int kRing = 2;
 template <int NT>
 struct ScanSmem {
     static constexpr int VS = 8 * NT;                        // value rows per CTA
+    // chunk intermediates in flight per CTA: three, two for 64 value rows (whose
+    // S and U rings take the room of the third)
+    static constexpr int kStages = NT >= 8 ? 2 : 3;
     static constexpr int kShared = kWsSharedBytes;           // w, qg, kg, aqk, gamma
     static constexpr int kSharedPad = round1k(kShared);
     static constexpr int kU = (VS / 16) * kWsUSliceBytes;    // the CTA's u columns
@@ -118,6 +120,7 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
                                           const WalkRange& R = WalkRange()) {
     using L = ScanSmem<NT>;
     constexpr int VS = L::VS;
+    constexpr int kStages = L::kStages;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBar);  // [kStages]
     uint64_t* empty = full + kStages;                               // [kStages]
     uint64_t* sready = full + 2 * kStages;                          // [kRing]
@@ -223,7 +226,7 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
                 uint32_t a[4];
                 ldsm_x4(tqg + sw128_off(16 * wr + rr + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1), 64),
                         a[0], a[1], a[2], a[3]);
-                float (*d)[4] = (ks & 1) ? acc2 : acc;
+                float (*d)[4] = (NT <= 4 && (ks & 1)) ? acc2 : acc;  // two chains for few n-tiles
 #pragma unroll
                 for (int np = 0; np < NT / 2; ++np) {
                     uint32_t bb[4];
@@ -332,16 +335,22 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
             }
     };
     // B fragments of S for U = w S^T: [ks][nt][b0, b1]
-    uint32_t Sf[8][NT][2];
+    // S as the B operand of U = w S^T, [ks][nt][b0, b1]: loaded once after S is
+    // published for up to 32 value rows; with 64 the fragments are loaded per
+    // K step inside the product instead (they would take 128 registers)
+    constexpr bool kHoldS = NT <= 4;
+    uint32_t Sf[kHoldS ? 8 : 1][NT][2];
     auto load_sfrag = [&](int b) {
-        const uint32_t s16 = s16_slot(b);
+        if constexpr (kHoldS) {
+            const uint32_t s16 = s16_slot(b);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
+            for (int ks = 0; ks < 8; ++ks)
 #pragma unroll
-            for (int np = 0; np < NT / 2; ++np)
-                ldsm_x4(s16 + sw128_off(16 * np + rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1), VS),
-                        Sf[ks][2 * np][0], Sf[ks][2 * np][1], Sf[ks][2 * np + 1][0],
-                        Sf[ks][2 * np + 1][1]);
+                for (int np = 0; np < NT / 2; ++np)
+                    ldsm_x4(s16 + sw128_off(16 * np + rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1), VS),
+                            Sf[ks][2 * np][0], Sf[ks][2 * np][1], Sf[ks][2 * np + 1][0],
+                            Sf[ks][2 * np + 1][1]);
+        }
     };
 
     write_s16(0);
@@ -358,16 +367,30 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
         const uint32_t tu = st + L::kSharedPad;  // [VS/16][64][16] fp16
         const uint32_t ut = ut_slot(b);
 
-        // U = u - w S^T for chunk rows 16wr..16wr+15 (two chains over the key halves)
-        float accU[NT][4] = {}, accU2[NT][4] = {};
+        // U = u - w S^T for chunk rows 16wr..16wr+15 (two chains over the key halves
+        // while there are few n-tiles)
+        constexpr int kUChains = NT <= 4 ? 2 : 1;
+        float accU[NT][4] = {}, accU2[kUChains == 2 ? NT : 1][4] = {};
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             uint32_t a[4];
             ldsm_x4(tw + sw128_off(16 * wr + rr + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1), 64), a[0],
                     a[1], a[2], a[3]);
-            float (*d)[4] = (ks & 1) ? accU2 : accU;
+            if constexpr (kHoldS) {
+                float (*d)[4] = (kUChains == 2 && (ks & 1)) ? accU2 : accU;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_f16(d[nt], a, Sf[ks][nt][0], Sf[ks][nt][1]);
+                for (int nt = 0; nt < NT; ++nt) mma_f16(d[nt], a, Sf[ks][nt][0], Sf[ks][nt][1]);
+            } else {
+                const uint32_t s16 = s16_slot(b);
+#pragma unroll
+                for (int np = 0; np < NT / 2; ++np) {
+                    uint32_t sb4[4];
+                    ldsm_x4(s16 + sw128_off(16 * np + rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1), VS),
+                            sb4[0], sb4[1], sb4[2], sb4[3]);
+                    mma_f16(accU[2 * np], a, sb4[0], sb4[1]);
+                    mma_f16(accU[2 * np + 1], a, sb4[2], sb4[3]);
+                }
+            }
         }
         uint32_t uf[NT][2];  // U as fp16 pairs: [nt][rows g, g + 8]
 #pragma unroll
@@ -382,8 +405,12 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
                              : "r"(tu + (vv >> 4) * kWsUSliceBytes + (i * 16 + (vv & 15)) * 2));
                 const float2 u2 = R.zero_u ? make_float2(0.f, 0.f)
                                            : __half22float2(*reinterpret_cast<__half2*>(&uv));
-                uf[nt][hh] = pack_half2(u2.x - accU[nt][2 * hh] - accU2[nt][2 * hh],
-                                        u2.y - accU[nt][2 * hh + 1] - accU2[nt][2 * hh + 1]);
+                float x0 = u2.x - accU[nt][2 * hh], x1 = u2.y - accU[nt][2 * hh + 1];
+                if constexpr (kUChains == 2) {
+                    x0 -= accU2[nt][2 * hh];
+                    x1 -= accU2[nt][2 * hh + 1];
+                }
+                uf[nt][hh] = pack_half2(x0, x1);
             }
         // U^T into ring slot b (rows v, columns c): stmatrix transposes 8x8 blocks
 #pragma unroll
@@ -394,42 +421,64 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
                       uf[2 * np + 1][1]);
         }
         // kg^T fragments of the update, loaded before the barrier (they do not
-        // depend on U) so that their latency overlaps the wait
-        uint32_t kga[4][2][4];
+        // depend on U) so that their latency overlaps the wait; for 64 value rows
+        // per K step of each half instead (registers)
+        auto load_kga = [&](int ks, int mt, uint32_t (&f)[4]) {
+            ldsm_x4_t(tkg + sw128_off(16 * ks + rr + 8 * (mi >> 1), 32 * wr + 16 * mt + 8 * (mi & 1), 64),
+                      f[0], f[1], f[2], f[3]);
+        };
+        constexpr bool kHoldKg = NT <= 4;
+        uint32_t kga[kHoldKg ? 4 : 1][2][4];
+        if constexpr (kHoldKg) {
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
+            for (int ks = 0; ks < 4; ++ks)
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
-                ldsm_x4_t(tkg + sw128_off(16 * ks + rr + 8 * (mi >> 1), 32 * wr + 16 * mt + 8 * (mi & 1), 64),
-                          kga[ks][mt][0], kga[ks][mt][1], kga[ks][mt][2], kga[ks][mt][3]);
+                for (int mt = 0; mt < 2; ++mt) load_kga(ks, mt, kga[ks][mt]);
+        }
         const int abort1 = state_sync_flag(!ok);  // a copy never landed (tested below)
         if (tid == 0) mbar_arrive(&sready[b]);  // S (published last step) and U of this chunk
 
-        // dS^T = kg^T U for key channels 32wr..32wr+31; S = gamma S + dS
-        float accS[2][NT][4] = {};
+        // dS^T = kg^T U for key channels 32wr..32wr+31; S = gamma S + dS (for 64
+        // value rows in two halves of 32, which keeps the accumulators in registers)
+        constexpr int kVH = NT >= 8 ? 2 : 1, NTH = NT / kVH;
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            uint32_t bb[NT][2];
+        for (int vh = 0; vh < kVH; ++vh) {
+            float accS[2][NTH][4] = {};
 #pragma unroll
-            for (int np = 0; np < NT / 2; ++np)
-                ldsm_x4(ut + sw64_off(16 * np + rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1)),
-                        bb[2 * np][0], bb[2 * np][1], bb[2 * np + 1][0], bb[2 * np + 1][1]);
+            for (int ks = 0; ks < 4; ++ks) {
+                uint32_t bb[NTH][2];
+#pragma unroll
+                for (int np = 0; np < NTH / 2; ++np)
+                    ldsm_x4(ut + sw64_off(16 * (vh * NTH / 2 + np) + rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1)),
+                            bb[2 * np][0], bb[2 * np][1], bb[2 * np + 1][0], bb[2 * np + 1][1]);
+                uint32_t ka[2][4];
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    if constexpr (kHoldKg) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) ka[mt][e] = kga[ks][mt][e];
+                    } else {
+                        load_kga(ks, mt, ka[mt]);
+                    }
+                }
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < NTH; ++nt) mma_f16(accS[mt][nt], ka[mt], bb[nt][0], bb[nt][1]);
+            }
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma_f16(accS[mt][nt], kga[ks][mt], bb[nt][0], bb[nt][1]);
-        }
+                for (int hh = 0; hh < 2; ++hh) {
+                    const float gk = gam[32 * wr + 16 * mt + g + 8 * hh];
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const float gk = gam[32 * wr + 16 * mt + g + 8 * hh];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    Sm[mt][nt][2 * hh] = gk * Sm[mt][nt][2 * hh] + accS[mt][nt][2 * hh];
-                    Sm[mt][nt][2 * hh + 1] = gk * Sm[mt][nt][2 * hh + 1] + accS[mt][nt][2 * hh + 1];
+                    for (int nt = 0; nt < NTH; ++nt) {
+                        const int n2 = vh * NTH + nt;
+                        Sm[mt][n2][2 * hh] = gk * Sm[mt][n2][2 * hh] + accS[mt][nt][2 * hh];
+                        Sm[mt][n2][2 * hh + 1] = gk * Sm[mt][n2][2 * hh + 1] + accS[mt][nt][2 * hh + 1];
+                    }
                 }
-            }
+        }
         if (abort1) {  // report, stop the walk
             failed = true;
             if (tid == 0 && p.status) atomicOr(p.status, 1);

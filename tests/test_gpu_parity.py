@@ -41,9 +41,13 @@ CASES = [
     ([8, 9, 1, 0, 7, 2, 64, 3], 2, torch.float32, 32),
     ([3] * 5 + [1] * 5 + [8], 3, torch.float16, 0),
     # more than 2 * SMs / 8 (sequence, head) pairs on a 152-SM GPU: the scan's
-    # large-batch form (32 value rows per CTA)
+    # large-batch form (64 value rows per CTA: S and kg fragments loaded per K
+    # step, the update in two halves, two stages), with one wave of CTAs and with
+    # more than one
     ([70, 9, 128, 200, 65, 150, 33, 99, 64, 300] * 2, 2, torch.float32, 0),
     ([130, 65, 10, 257, 64] * 4, 2, torch.bfloat16, 64),
+    ([70, 9, 128, 200, 65, 150, 33, 99, 64, 300] * 4, 2, torch.float32, 0),
+    ([130, 65, 10, 257, 64] * 8, 2, torch.bfloat16, 64),
     # many short sequences: each persistent token-by-token CTA takes several items,
     # so its ring of state stages wraps around more than once
     ([1] * 300 + [2, 0, 5, 8] * 20, 2, torch.bfloat16, 0),
