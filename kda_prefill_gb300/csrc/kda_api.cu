@@ -517,6 +517,7 @@ int run_forward(const void* q, const void* k, const void* v, const void* g_raw,
     p.ws = ws ? ws + kda::kWsHeader : nullptr;
     p.status = ws ? reinterpret_cast<int*>(ws) : nullptr;
     p.queue = ws ? reinterpret_cast<int*>(ws + kda::kWsQueueOff) : nullptr;
+    p.dec_queue = ws ? reinterpret_cast<int*>(ws + kda::kWsDecodeOff) : nullptr;
     p.ready = ws ? reinterpret_cast<int*>(ws + kda::flags_offset(max_chunks(T, N), H)) : nullptr;
     p.seg = ws ? reinterpret_cast<float*>(ws + kda::seg_offset(max_chunks(T, N), H)) : nullptr;
     p.max_long_chunks = m->layout.max_long_chunks;
@@ -532,8 +533,8 @@ int run_forward(const void* q, const void* k, const void* v, const void* g_raw,
     (void)workspace_bytes;
 
     if (p.status) {
-        // the status word and the fused launch's work counter, one memset
-        e = cudaMemsetAsync(p.status, 0, kda::kWsQueueOff + sizeof(int), stream);
+        // the status word and the two work counters, one memset
+        e = cudaMemsetAsync(p.status, 0, kda::kWsClearBytes, stream);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (status)");
     }
     cudaEvent_t* marks = nullptr;
@@ -1075,7 +1076,7 @@ extern "C" int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v
     int32_t* sht = lng + align4((size_t)num_seqs);
 
     // the status word and the fused launch's work counter
-    cudaError_t e = cudaMemsetAsync(base, 0, kda::kWsQueueOff + sizeof(int), stream);
+    cudaError_t e = cudaMemsetAsync(base, 0, kda::kWsClearBytes, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (status)");
     if (num_seqs > 0) {
         HostPlan hp{total_tokens, bound, n_chunks, n_long, max_long,
@@ -1109,6 +1110,7 @@ extern "C" int kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v
     p.ws = base + kda::kWsHeader;
     p.status = reinterpret_cast<int*>(base);
     p.queue = reinterpret_cast<int*>(base + kda::kWsQueueOff);
+    p.dec_queue = reinterpret_cast<int*>(base + kda::kWsDecodeOff);
     p.ready = reinterpret_cast<int*>(base + kda::flags_offset(bound, num_heads));
     p.seg = reinterpret_cast<float*>(base + kda::seg_offset(bound, num_heads));
     p.max_long_chunks = max_long;

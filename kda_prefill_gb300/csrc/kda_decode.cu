@@ -104,6 +104,8 @@ constexpr int kItemRows = 64;
 constexpr int kConsumers = 128;                 // 4 compute warps, one thread per key
 constexpr int kDecThreadsAll = kConsumers + 32;  // + the producer warp
 static_assert(kConsumers == D, "the per-token prep maps compute threads to keys");
+constexpr int kClaim = 8;    // items per claim from the shared counter
+constexpr int kEnd = -2;     // StageHeader::len of the end marker
 struct StageHeader {
     int tok0, len, has_init, h, vb, pad;
     long long out_slot;
@@ -154,14 +156,32 @@ __global__ void __launch_bounds__(kDecThreadsAll, 3) kda_decode(FwdParams p, lon
     __syncthreads();
 
     // ======================= producer warp ==================================
+    // The CTA's items: with p.dec_queue, batches of kClaim consecutive items taken
+    // from the shared counter (CTAs that start late, e.g. beside the scan, take
+    // what is left); without it, items blockIdx.x + i * gridDim.x.  After the
+    // last item the next stage gets an end marker (len = kEnd, no copy).
     if (warp == kConsumers / 32) {
-        for (int base = 0;; base += 32) {
-            // lane i resolves the routing of the CTA's item base + i
-            const long long my_it = blockIdx.x + (long long)(base + lane) * gridDim.x;
+        const bool dyn = p.dec_queue != nullptr;
+        int r = 0;  // stage sequence number
+        for (long long base = 0;;) {
+            long long first = 0, stride = 1;
+            int cnt = kClaim;
+            if (dyn) {
+                int b0 = 0;
+                if (lane == 0) b0 = atomicAdd(p.dec_queue, kClaim);
+                first = __shfl_sync(0xffffffffu, b0, 0);
+            } else {
+                first = blockIdx.x + base * gridDim.x;
+                stride = gridDim.x;
+                cnt = 32;
+                base += 32;
+            }
+            // lane i resolves the routing of item first + i * stride
+            const long long my_it = first + (long long)lane * stride;
             int n = 0, h = 0, vb = 0, tok0 = 0, len = 0, init = 0;
             long long in_slot = 0, out_slot = 0;
             float braw = 0.f;
-            if (my_it < n_items) {
+            if (lane < cnt && my_it < n_items) {
                 const long long sh = my_it >> 1;
                 vb = kItemRows * (int)(my_it & 1);
                 h = (int)(sh % H);
@@ -181,12 +201,8 @@ __global__ void __launch_bounds__(kDecThreadsAll, 3) kda_decode(FwdParams p, lon
                 if (len > 0) braw = load_raw(p.beta_raw, p.raw_bf16, (size_t)tok0 * H + h);
             }
             bool stop = false;
-            for (int j = 0; j < 32; ++j) {
-                const int r = base + j;
-                if (blockIdx.x + (long long)r * gridDim.x >= n_items) {
-                    stop = true;
-                    break;
-                }
+            for (int j = 0; j < cnt; ++j, ++r) {
+                const bool end = first + (long long)j * stride >= n_items;
                 const int jh = __shfl_sync(0xffffffffu, h, j);
                 const int jvb = __shfl_sync(0xffffffffu, vb, j);
                 const int jtok0 = __shfl_sync(0xffffffffu, tok0, j);
@@ -199,6 +215,11 @@ __global__ void __launch_bounds__(kDecThreadsAll, 3) kda_decode(FwdParams p, lon
                     const int st = r % stages;
                     if (r >= stages && !mbar_wait(&empty[st], (uint32_t)(((r / stages) - 1) & 1))) {
                         if (p.status) atomicOr(p.status, 1);
+                        stop = true;
+                    } else if (end) {
+                        uint8_t* stg = ring + st * sbytes;
+                        reinterpret_cast<StageHeader*>(stg + tile + kHdrOff)->len = kEnd;
+                        mbar_arrive(&full[st]);  // the end marker: nothing to copy
                         stop = true;
                     } else {
                         uint8_t* stg = ring + st * sbytes;
@@ -262,20 +283,19 @@ __global__ void __launch_bounds__(kDecThreadsAll, 3) kda_decode(FwdParams p, lon
     };
 
     for (int r = 0;; ++r) {
-        if (blockIdx.x + (long long)r * gridDim.x >= n_items) break;
         const int st = r % stages;
         const bool ok = mbar_wait(&full[st], (uint32_t)((r / stages) & 1));
         if (csync_or(!ok)) {  // a copy never landed: report, leave together
             if (tid == 0) {
                 if (p.status) atomicOr(p.status, 1);
                 for (int rq = r; rq < r + stages; ++rq)  // copies possibly in flight, bounded
-                    if (blockIdx.x + (long long)rq * gridDim.x < n_items)
-                        mbar_wait(&full[rq % stages], (uint32_t)((rq / stages) & 1));
+                    mbar_wait(&full[rq % stages], (uint32_t)((rq / stages) & 1));
             }
             return;
         }
         const uint8_t* stg = ring + st * sbytes;
         const StageHeader* hd = reinterpret_cast<const StageHeader*>(stg + tile + kHdrOff);
+        if (hd->len == kEnd) break;  // the producer's end marker
         const int tok0 = hd->tok0, len = hd->len, h = hd->h, vb = hd->vb;
         const bool has_init = hd->has_init != 0;
         const bool store_ok = hd->out_slot >= 0;
@@ -392,11 +412,15 @@ __global__ void __launch_bounds__(kDecThreadsAll, 3) kda_decode(FwdParams p, lon
             }
         }
     }
+    // Launched beside the scan (programmatic stream serialization), this grid
+    // completes only after the scan has: later work on the stream sees both.
+    // Without such a predecessor the wait returns at once.
+    if (tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const FwdParams& p, cudaStream_t s) {
+cudaError_t launch_decode(const FwdParams& p, cudaStream_t s, bool beside_scan) {
     if (p.n_short <= 0 || !p.short_list) return cudaSuccess;
     // per device: the ring's shared memory allowance, and how many CTAs fit on
     // the GPU at once for each ring size (fp32 pool, 2-byte pool)
@@ -422,8 +446,21 @@ cudaError_t launch_decode(const FwdParams& p, cudaStream_t s) {
     }
     const long long n_items = 2LL * p.n_short * p.H;
     const unsigned grid = (unsigned)(n_items < ctas ? n_items : ctas);
-    kda_decode<<<grid, kDecThreadsAll, smem, s>>>(p, n_items);
-    return cudaGetLastError();
+    if (!beside_scan || !p.dec_queue) {
+        kda_decode<<<grid, kDecThreadsAll, smem, s>>>(p, n_items);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kDecThreadsAll);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kda_decode, p, n_items);
 }
 
 }  // namespace kda

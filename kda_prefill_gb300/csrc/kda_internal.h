@@ -34,12 +34,16 @@ constexpr int kWsSharedBytes = 57856;
 constexpr int kWsUOff = 57856;
 constexpr int kWsUSliceBytes = 2048;
 constexpr int kWsBytes = 74240;
-// Workspace header: one int status word (bit 0: a bounded wait gave up) and,
-// at byte kWsQueueOff, the work counter of the fused launch; the chunk blocks
-// start at kWsHeader.  After the blocks (bounded by max_chunks * H) come the
-// fused launch's ready flags, one int per (chunk, head) block.
+// Workspace header: one int status word (bit 0: a bounded wait gave up), at
+// byte kWsQueueOff the work counter of the fused launch and at kWsDecodeOff the
+// token-by-token kernel's item counter (all three cleared by one memset per
+// call); the chunk blocks start at kWsHeader.  After the blocks (bounded by
+// max_chunks * H) come the fused launch's ready flags, one int per (chunk, head)
+// block.
 constexpr int kWsHeader = 256;
 constexpr int kWsQueueOff = 64;
+constexpr int kWsDecodeOff = 68;
+constexpr int kWsClearBytes = kWsDecodeOff + 4;
 
 // Everything one forward launch sequence needs.  Device pointers unless noted.
 struct FwdParams {
@@ -72,6 +76,7 @@ struct FwdParams {
     uint8_t* ws;   // chunk blocks (kWsBytes each)
     int* status;   // workspace header
     int* queue;    // fused launch: work counter (workspace header)
+    int* dec_queue;  // token-by-token kernel: item counter (workspace header), or nullptr
     int* ready;    // fused launch: per (chunk, head) block, nonzero once it is written
 
     // state (paged: st_in == st_out == pool, idx = state_indices;
@@ -151,7 +156,11 @@ unsigned launched_kernels(const FwdParams& p);
 // Individual stages (kda_intra.cu, kda_scan.cu, kda_decode.cu).
 cudaError_t launch_intra(const FwdParams& p, cudaStream_t s);
 cudaError_t launch_scan(const FwdParams& p, int groups, cudaStream_t s);
-cudaError_t launch_decode(const FwdParams& p, cudaStream_t s);
+// beside_scan: launched right after the scan with programmatic stream
+// serialization, so that its CTAs take the SMs the scan's walks leave free (the
+// decode's items are other sequences, independent of the scan's); the decode
+// grid completes only after the scan has.
+cudaError_t launch_decode(const FwdParams& p, cudaStream_t s, bool beside_scan = false);
 // Fused intra + scan launch (kda_intra_tc.cu), used instead of the two when
 // fused_eligible(p): the walks need few enough SMs, the device takes a
 // cooperative launch of one CTA per SM, and p.ready / p.queue are set.

@@ -66,7 +66,10 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t s, cudaEvent_t* mark
         if (e != cudaSuccess) return e;
     }
     if (marks) cudaEventRecord(marks[3], s);
-    e = launch_decode(q, s);
+    // after the plain scan (not the fused launch, which fills the GPU, nor when
+    // the kernels are timed one by one), the token-by-token kernel runs beside it
+    const bool beside = !fused && !marks && n_scan_of(q) > 0 && q.n_chunks > 0;
+    e = launch_decode(q, s, beside);
     if (e != cudaSuccess) return e;
     if (marks) cudaEventRecord(marks[4], s);
     return cudaSuccess;

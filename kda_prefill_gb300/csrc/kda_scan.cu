@@ -36,6 +36,9 @@ namespace {
 // first sequences (the host orders it longest first) start in the first wave.
 template <int NT>
 __global__ void __launch_bounds__(scan::kScanThreads, 1) kda_scan_mma(FwdParams p) {
+    // a token-by-token grid launched after this one may start now: it takes the
+    // SMs the walks leave free (it waits for this grid before it completes)
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (call_aborted(p)) return;
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int kGroups = kD / scan::ScanSmem<NT>::VS;
