@@ -104,7 +104,7 @@ constexpr int kItemRows = 64;
 constexpr int kConsumers = 128;                 // 4 compute warps, one thread per key
 constexpr int kDecThreadsAll = kConsumers + 32;  // + the producer warp
 static_assert(kConsumers == D, "the per-token prep maps compute threads to keys");
-constexpr int kClaim = 8;    // items per claim from the shared counter
+constexpr int kClaim = 8;    // items per claim from the shared counter (1 near the end)
 constexpr int kEnd = -2;     // StageHeader::len of the end marker
 struct StageHeader {
     int tok0, len, has_init, h, vb, pad;
@@ -163,13 +163,16 @@ __global__ void __launch_bounds__(kDecThreadsAll, 3) kda_decode(FwdParams p, lon
     if (warp == kConsumers / 32) {
         const bool dyn = p.dec_queue != nullptr;
         int r = 0;  // stage sequence number
+        int claim = kClaim;
         for (long long base = 0;;) {
             long long first = 0, stride = 1;
-            int cnt = kClaim;
+            int cnt = claim;
             if (dyn) {
                 int b0 = 0;
-                if (lane == 0) b0 = atomicAdd(p.dec_queue, kClaim);
+                if (lane == 0) b0 = atomicAdd(p.dec_queue, claim);
                 first = __shfl_sync(0xffffffffu, b0, 0);
+                // near the end single items, so that the CTAs finish together
+                if (n_items - (first + claim) < (long long)gridDim.x * kClaim) claim = 1;
             } else {
                 first = blockIdx.x + base * gridDim.x;
                 stride = gridDim.x;
