@@ -129,7 +129,8 @@ __host__ __device__ constexpr int dec_smem(int dtype) {
 }
 constexpr int kDecSmemMax = dec_smem(1) > dec_smem(0) ? dec_smem(1) : dec_smem(0);
 
-__global__ void __launch_bounds__(kDecThreadsAll, 3) kda_decode(FwdParams p, long long n_items) {
+// The kernel's work; it may return early (an aborted call, a wait that gave up).
+__device__ __forceinline__ void decode_items(const FwdParams& p, long long n_items) {
     if (call_aborted(p)) return;
     extern __shared__ __align__(128) uint8_t ring[];  // stages, then mbarriers
     __shared__ __align__(16) float s_q[D], s_k[D], s_a[D];  // q^, k^, a of the token
@@ -415,10 +416,14 @@ __global__ void __launch_bounds__(kDecThreadsAll, 3) kda_decode(FwdParams p, lon
             }
         }
     }
+}
+
+__global__ void __launch_bounds__(kDecThreadsAll, 3) kda_decode(FwdParams p, long long n_items) {
+    decode_items(p, n_items);
     // Launched beside the scan (programmatic stream serialization), this grid
-    // completes only after the scan has: later work on the stream sees both.
-    // Without such a predecessor the wait returns at once.
-    if (tid == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+    // completes only after the scan has, however its CTAs left: later work on
+    // the stream sees both.  Without such a predecessor the wait returns at once.
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace
