@@ -106,21 +106,6 @@ __device__ __forceinline__ uint32_t tf32_bits(float x) {
     return (__float_as_uint(x) + 0x1000u) & 0xffffe000u;
 }
 
-__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-                 "r"(smem_u32(src)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_read_all() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // Marks a (chunk, head) block as written for the fused launch's scan walks: the
 // block's bulk stores have completed (cp.async.bulk.wait_group 0 by this
 // thread) and the CTA's other stores to it came before a CTA barrier.
@@ -839,16 +824,16 @@ EncodeTiledFn encode_fn() {
 }
 
 bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elt, int box_x,
-              int H, int64_t T) {
+              int H, int64_t T, int box_rows = C) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T};
     cuuint64_t strides[2] = {(cuuint64_t)128 * elt, (cuuint64_t)H * 128 * elt};
-    cuuint32_t box[3] = {(cuuint32_t)box_x, 1, (cuuint32_t)C};
+    cuuint32_t box[3] = {(cuuint32_t)box_x, 1, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool make_maps(IntraMaps* maps, const FwdParams& p) {
@@ -890,6 +875,13 @@ bool fused_device_ok() {
 }
 
 }  // namespace
+
+bool make_out_map(CUtensorMap* m, const FwdParams& p) {
+    // 16 rows of 64 values of one head: the rows one output warp of a 64-row
+    // walk forms per chunk (128-byte rows, swizzled like the walk's staging)
+    if (!p.out || (reinterpret_cast<uintptr_t>(p.out) & 15) != 0 || p.T <= 0) return false;
+    return make_map(m, p.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, p.H, p.T, 16);
+}
 
 static std::atomic<bool> g_fused_enabled{true};
 void set_fused_enabled(bool on) { g_fused_enabled.store(on); }

@@ -35,7 +35,8 @@ namespace {
 // slowest-varying index: CTAs start in launch order, so the walks of the list's
 // first sequences (the host orders it longest first) start in the first wave.
 template <int NT>
-__global__ void __launch_bounds__(scan::kScanThreads, 1) kda_scan_mma(FwdParams p) {
+__global__ void __launch_bounds__(scan::kScanThreads, 1)
+kda_scan_mma(FwdParams p, const __grid_constant__ CUtensorMap out_map, int has_out_map) {
     // a token-by-token grid launched after this one may start now: it takes the
     // SMs the walks leave free (it waits for this grid before it completes)
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -45,7 +46,7 @@ __global__ void __launch_bounds__(scan::kScanThreads, 1) kda_scan_mma(FwdParams 
     const int b = (int)blockIdx.x;
     const int z = b % kGroups, h = (b / kGroups) % p.H, sq = b / (kGroups * p.H);
     const int n = p.long_list ? p.long_list[sq] : sq;
-    scan::scan_walk<NT>(p, smem, n, h, z);
+    scan::scan_walk<NT>(p, smem, n, h, z, scan::WalkRange(), has_out_map ? &out_map : nullptr);
 }
 
 // ---- segmented scan --------------------------------------------------------
@@ -247,7 +248,9 @@ cudaError_t launch_scan_nt(const FwdParams& p, cudaStream_t s) {
     const int n_seq = p.long_list ? p.n_long : p.N;
     if (n_seq <= 0) return cudaSuccess;
     const long blocks = (long)n_seq * p.H * (kD / L::VS);
-    kda_scan_mma<NT><<<(unsigned)blocks, scan::kScanThreads, L::kTotal, s>>>(p);
+    CUtensorMap out_map = {};
+    const int has_out_map = (L::kOutBufs > 0 && make_out_map(&out_map, p)) ? 1 : 0;
+    kda_scan_mma<NT><<<(unsigned)blocks, scan::kScanThreads, L::kTotal, s>>>(p, out_map, has_out_map);
     return cudaGetLastError();
 }
 

@@ -69,7 +69,16 @@ struct ScanSmem {
     static constexpr int kS16Slot = VS * 256;
     static constexpr int kUt = kS16 + kRing * kS16Slot;      // kRing slots x [VS][64] fp16
     static constexpr int kUtSlot = VS * 128;
-    static constexpr int kBar = kUt + kRing * kUtSlot;       // mbarriers (2 kStages + 2 kRing)
+    // output staging for the TMA stores of `out`: per output warp kOutBufs buffers
+    // of its 16 chunk rows x VS values (bf16, 128-byte swizzled rows).  Only the
+    // 64-row walks store this way: for 16 rows the stores measured slower (the
+    // 16K prefill's scan 204 against 182 us), for 64 faster (varlen batch 567
+    // against 582 us, mixed batch 63.5 against 65.9).
+    static constexpr int kOutBufs = NT >= 8 ? 2 : 0;
+    static constexpr int kOutBuf = 16 * VS * 2;
+    static constexpr int kOutWarpsN = 4;
+    static constexpr int kOut = round1k(kUt + kRing * kUtSlot);
+    static constexpr int kBar = kOut + kOutWarpsN * kOutBufs * kOutBuf;  // mbarriers (2 kStages + 2 kRing)
     static constexpr int kAbort = kBar + 8 * (2 * kStages + 2 * kRing);  // int: a state warp gave up
     static constexpr int kTotal = kBar + 128;
     static_assert(kAbort + 4 <= kTotal, "mbarriers and the abort flag fit");
@@ -115,9 +124,13 @@ struct WalkRange {
     float* final_buf = nullptr;   // ... into this [128][128] fp32 plane instead of the pool
 };
 
+// out_map (64-row walks only): a tensor map of `out` ([T][H][128] bf16, box 64
+// values x 1 head x 16 rows, 128-byte swizzle) for TMA stores of whole chunks'
+// outputs, or nullptr (every output row stored directly).
 template <int NT>
 __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int n, int h, int z,
-                                          const WalkRange& R = WalkRange()) {
+                                          const WalkRange& R = WalkRange(),
+                                          const CUtensorMap* out_map = nullptr) {
     using L = ScanSmem<NT>;
     constexpr int VS = L::VS;
     constexpr int kStages = L::kStages;
@@ -256,20 +269,57 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
                 mbar_arrive(&sfree[b]);
                 mbar_arrive(&empty[sg]);
             }
+            bool staged = false;
+            if constexpr (L::kOutBufs > 0) {
+                if (R.outputs && out_map && lc * C + C <= len) {
+                    // a whole chunk: the warp's 16 rows into its staging buffer
+                    // (bf16), then one TMA store; the buffer was last read
+                    // kOutBufs chunks back
+                    staged = true;
+                    const uint32_t ob =
+                        sm_base + L::kOut + (L::kOutBufs * wr + lc % L::kOutBufs) * L::kOutBuf;
+                    if (lane == 0) bulk_wait_read<L::kOutBufs - 1>();
+                    __syncwarp();
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int i = 16 * wr + g + 8 * hh;
-                if (R.outputs && lc * C + i < len) {
-                    const size_t t = (size_t)(tok0 + lc * C + i);
-                    __nv_bfloat16* orow = p.out + (t * p.H + h) * D + v0;
+                    for (int np = 0; np < NT / 2; ++np) {
+                        const int row = rr + 8 * (mi & 1), col = 16 * np + 8 * (mi >> 1);
+                        uint32_t pv[4];
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const uint32_t pv = pack_bf162(acc[nt][2 * hh] + acc2[nt][2 * hh],
-                                                       acc[nt][2 * hh + 1] + acc2[nt][2 * hh + 1]);
-                        *reinterpret_cast<uint32_t*>(orow + 8 * nt + 2 * tq) = pv;
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const int nt = 2 * np + (q4 >> 1), hh = q4 & 1;
+                            pv[q4] = pack_bf162(acc[nt][2 * hh] + acc2[nt][2 * hh],
+                                                acc[nt][2 * hh + 1] + acc2[nt][2 * hh + 1]);
+                        }
+                        stsm_x4(ob + sw64_off(row, col), pv[0], pv[1], pv[2], pv[3]);
+                    }
+                    fence_proxy_async();  // the staged rows are read by the TMA store
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(out_map, smem + (ob - sm_base), v0, h, tok0 + lc * C + 16 * wr);
+                        bulk_commit();
                     }
                 }
             }
+            if (!staged) {  // each row of `out` directly (within the sequence)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int i = 16 * wr + g + 8 * hh;
+                    if (R.outputs && lc * C + i < len) {
+                        const size_t t = (size_t)(tok0 + lc * C + i);
+                        __nv_bfloat16* orow = p.out + (t * p.H + h) * D + v0;
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const uint32_t pv = pack_bf162(acc[nt][2 * hh] + acc2[nt][2 * hh],
+                                                           acc[nt][2 * hh + 1] + acc2[nt][2 * hh + 1]);
+                            *reinterpret_cast<uint32_t*>(orow + 8 * nt + 2 * tq) = pv;
+                        }
+                    }
+                }
+            }
+        }
+        // the TMA stores have completed before the CTA's shared memory is released
+        if constexpr (L::kOutBufs > 0) {
+            if (lane == 0) bulk_wait_all();
         }
         return;
     }
