@@ -174,10 +174,10 @@ bool fused_eligible(const FwdParams& p);
 void set_fused_enabled(bool on);
 cudaError_t launch_fused(const FwdParams& p, cudaStream_t s);
 int num_sms();
-int scan_groups(int N, int H, int num_sms);
-// A tensor map of `out` for the 64-row walks' TMA stores (box 64 values x 1
-// head x 16 rows); false when it cannot be made (the walks then store directly).
-bool make_out_map(CUtensorMap* m, const FwdParams& p);
+int scan_groups(int N, int H, int num_sms, int beside_pairs = 0);
+// A tensor map of `out` for a walk's TMA stores (box box_values values x 1 head
+// x box_rows rows); false when it cannot be made (the walk then stores directly).
+bool make_out_map(CUtensorMap* m, const FwdParams& p, int box_values, int box_rows);
 // Segments per long sequence when the scan runs segmented (few (sequence, head)
 // pairs, so that the segments' walks fill the GPU), else 0; *L = chunks per segment.
 int scan_segments(const FwdParams& p, int num_sms, int* L);

@@ -824,7 +824,8 @@ EncodeTiledFn encode_fn() {
 }
 
 bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elt, int box_x,
-              int H, int64_t T, int box_rows = C) {
+              int H, int64_t T, int box_rows = C,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T};
@@ -832,7 +833,7 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elt,
     cuuint32_t box[3] = {(cuuint32_t)box_x, 1, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -876,11 +877,11 @@ bool fused_device_ok() {
 
 }  // namespace
 
-bool make_out_map(CUtensorMap* m, const FwdParams& p) {
-    // 16 rows of 64 values of one head: the rows one output warp of a 64-row
-    // walk forms per chunk (128-byte rows, swizzled like the walk's staging)
+bool make_out_map(CUtensorMap* m, const FwdParams& p, int box_values, int box_rows) {
+    // box_rows rows of box_values values of one head, dense in shared memory
     if (!p.out || (reinterpret_cast<uintptr_t>(p.out) & 15) != 0 || p.T <= 0) return false;
-    return make_map(m, p.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, p.H, p.T, 16);
+    return make_map(m, p.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, box_values, p.H, p.T, box_rows,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 static std::atomic<bool> g_fused_enabled{true};

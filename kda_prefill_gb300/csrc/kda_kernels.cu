@@ -32,6 +32,14 @@ unsigned launched_kernels(const FwdParams& p) {
 
 static int n_scan_of(const FwdParams& p) { return p.long_list ? p.n_long : p.N; }
 
+// The scan's value-row split for this call; it counts the token-by-token
+// kernel's (sequence, head) pairs, which run beside the scan.  The split does
+// not depend on whether the kernels are timed one by one.
+static int groups_of(const FwdParams& p) {
+    const int beside = p.short_list && p.n_short > 0 ? p.n_short * p.H : 0;
+    return scan_groups(n_scan_of(p), p.H, num_sms(), beside);
+}
+
 cudaError_t launch_forward(const FwdParams& p, cudaStream_t s, cudaEvent_t* marks) {
     cudaError_t e;
     const bool fused = fused_eligible(p);
@@ -45,8 +53,7 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t s, cudaEvent_t* mark
     }
     if (marks) cudaEventRecord(marks[1], s);
     if (!fused) {
-        const int n_scan = q.long_list ? q.n_long : q.N;
-        e = launch_scan(q, scan_groups(n_scan, q.H, num_sms()), s);
+        e = launch_scan(q, groups_of(q), s);
         if (e != cudaSuccess) return e;
     }
     if (marks) cudaEventRecord(marks[2], s);
@@ -60,7 +67,7 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t s, cudaEvent_t* mark
             if (marks) cudaEventRecord(marks[0], s);
             e = launch_intra(q, s);
             if (marks) cudaEventRecord(marks[1], s);
-            if (e == cudaSuccess) e = launch_scan(q, scan_groups(n_scan_of(q), q.H, num_sms()), s);
+            if (e == cudaSuccess) e = launch_scan(q, groups_of(q), s);
             if (marks) cudaEventRecord(marks[2], s);
         }
         if (e != cudaSuccess) return e;

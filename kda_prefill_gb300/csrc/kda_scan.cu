@@ -25,8 +25,13 @@
 // synchronise among themselves on a named barrier.  Products are warp-level
 // tensor-core MMAs (m16n8k16, fp16 operands, fp32 accumulation); fp16 tiles
 // are written with stmatrix (transposing) and read with ldmatrix.
+//
+// This role split serves 16 value rows per CTA, for batches with few (sequence,
+// head) pairs.  Batches with more pairs take 64 or 128 value rows per CTA in the
+// values-partitioned walk of kda_scan_vp.cuh, where each warp owns its value
+// rows for all keys and no state crosses between warps.
 
-#include "kda_scan_walk.cuh"
+#include "kda_scan_vp.cuh"
 
 namespace kda {
 namespace {
@@ -36,7 +41,7 @@ namespace {
 // first sequences (the host orders it longest first) start in the first wave.
 template <int NT>
 __global__ void __launch_bounds__(scan::kScanThreads, 1)
-kda_scan_mma(FwdParams p, const __grid_constant__ CUtensorMap out_map, int has_out_map) {
+kda_scan_mma(FwdParams p) {
     // a token-by-token grid launched after this one may start now: it takes the
     // SMs the walks leave free (it waits for this grid before it completes)
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -46,7 +51,7 @@ kda_scan_mma(FwdParams p, const __grid_constant__ CUtensorMap out_map, int has_o
     const int b = (int)blockIdx.x;
     const int z = b % kGroups, h = (b / kGroups) % p.H, sq = b / (kGroups * p.H);
     const int n = p.long_list ? p.long_list[sq] : sq;
-    scan::scan_walk<NT>(p, smem, n, h, z, scan::WalkRange(), has_out_map ? &out_map : nullptr);
+    scan::scan_walk<NT>(p, smem, n, h, z);
 }
 
 // ---- segmented scan --------------------------------------------------------
@@ -248,21 +253,63 @@ cudaError_t launch_scan_nt(const FwdParams& p, cudaStream_t s) {
     const int n_seq = p.long_list ? p.n_long : p.N;
     if (n_seq <= 0) return cudaSuccess;
     const long blocks = (long)n_seq * p.H * (kD / L::VS);
+    kda_scan_mma<NT><<<(unsigned)blocks, scan::kScanThreads, L::kTotal, s>>>(p);
+    return cudaGetLastError();
+}
+
+// One CTA per (long sequence, head, 16 NW value rows), sequence-major like
+// kda_scan_mma: the values-partitioned walk of kda_scan_vp.cuh.
+template <int NW>
+__global__ void __launch_bounds__(scan::vp_threads<NW>(), 1)
+kda_scan_vp(FwdParams p, const __grid_constant__ CUtensorMap out_map, int has_out_map) {
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (call_aborted(p)) return;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    constexpr int kGroups = kD / scan::ScanSmemVP<NW>::VS;
+    const int b = (int)blockIdx.x;
+    const int z = b % kGroups, h = (b / kGroups) % p.H, sq = b / (kGroups * p.H);
+    const int n = p.long_list ? p.long_list[sq] : sq;
+    scan::scan_walk_vp<NW>(p, smem, n, h, z, has_out_map ? &out_map : nullptr);
+}
+
+template <int NW>
+cudaError_t launch_scan_vp(const FwdParams& p, cudaStream_t s) {
+    using L = scan::ScanSmemVP<NW>;
+    static unsigned configured = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 32 && !(configured & (1u << dev))) {
+        e = cudaFuncSetAttribute(kda_scan_vp<NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 L::kTotal);
+        if (e != cudaSuccess) return e;
+        configured |= 1u << dev;
+    }
+    const int n_seq = p.long_list ? p.n_long : p.N;
+    if (n_seq <= 0) return cudaSuccess;
+    const long blocks = (long)n_seq * p.H * (kD / L::VS);
     CUtensorMap out_map = {};
-    const int has_out_map = (L::kOutBufs > 0 && make_out_map(&out_map, p)) ? 1 : 0;
-    kda_scan_mma<NT><<<(unsigned)blocks, scan::kScanThreads, L::kTotal, s>>>(p, out_map, has_out_map);
+    const int has_out_map = make_out_map(&out_map, p, 16, kC) ? 1 : 0;
+    kda_scan_vp<NW><<<(unsigned)blocks, scan::vp_threads<NW>(), L::kTotal, s>>>(p, out_map,
+                                                                               has_out_map);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-int scan_groups(int N, int H, int num_sms) {
+int scan_groups(int N, int H, int num_sms, int beside_pairs) {
     // 16 value rows per CTA while (sequence, head) pairs are few enough for the
-    // finer split to fill the GPU, else 64: the head-wide chunk operands each CTA
-    // reads then serve four times as many value rows (measured against 32 rows
-    // per CTA: mixed batch 70.3 against 76.6 us, varlen batch 620 against 699 us).
+    // finer split to fill the GPU, else 64 or 128: the head-wide chunk operands
+    // each CTA reads then serve four or eight times as many value rows (64 rows
+    // against 32: mixed batch 70.3 against 76.6 us, varlen batch 620 against
+    // 699 us).  Walks of 64 rows while they fit one wave; walks of 128 rows
+    // past that, and also when a token-by-token kernel with at least a wave of
+    // (sequence, head) pairs runs beside the scan: half as many scan CTAs leave
+    // it the other SMs (mixed batch of 4 x 2048 prefill tokens and 512 decode
+    // tokens: 198.5 against 203.4 us per call).
     const long pairs = (long)N * H;
-    return pairs * 8 <= 2L * num_sms ? 1 : 4;
+    if (pairs * 8 <= 2L * num_sms) return 1;
+    return pairs * 2 <= num_sms && beside_pairs < num_sms ? 4 : 8;
 }
 
 int scan_segments(const FwdParams& p, int num_sms, int* L) {
@@ -285,7 +332,8 @@ cudaError_t launch_scan(const FwdParams& p, int groups, cudaStream_t s) {
     int L = 0;
     const int P = scan_segments(p, num_sms(), &L);
     if (P > 0) return launch_scan_segmented(p, P, L, s);
-    return groups <= 1 ? launch_scan_nt<2>(p, s) : launch_scan_nt<8>(p, s);
+    if (groups <= 1) return launch_scan_nt<2>(p, s);
+    return groups == 4 ? launch_scan_vp<4>(p, s) : launch_scan_vp<8>(p, s);
 }
 
 }  // namespace kda

@@ -55,12 +55,13 @@ constexpr int kPrefetch = 6;  // chunks ahead of the stage loads asked of L2
 // slower: 188 against 183 us for the 16K prefill's scan).
 constexpr int kRing = 2;
 
+// The role-split walk serves 16 or 32 value rows per CTA; larger blocks of
+// value rows take the values-partitioned walk (kda_scan_vp.cuh).
 template <int NT>
 struct ScanSmem {
+    static_assert(NT == 2 || NT == 4, "16 or 32 value rows per CTA");
     static constexpr int VS = 8 * NT;                        // value rows per CTA
-    // chunk intermediates in flight per CTA: three, two for 64 value rows (whose
-    // S and U rings take the room of the third)
-    static constexpr int kStages = NT >= 8 ? 2 : 3;
+    static constexpr int kStages = 3;                        // chunk intermediates in flight
     static constexpr int kShared = kWsSharedBytes;           // w, qg, kg, aqk, gamma
     static constexpr int kSharedPad = round1k(kShared);
     static constexpr int kU = (VS / 16) * kWsUSliceBytes;    // the CTA's u columns
@@ -69,16 +70,9 @@ struct ScanSmem {
     static constexpr int kS16Slot = VS * 256;
     static constexpr int kUt = kS16 + kRing * kS16Slot;      // kRing slots x [VS][64] fp16
     static constexpr int kUtSlot = VS * 128;
-    // output staging for the TMA stores of `out`: per output warp kOutBufs buffers
-    // of its 16 chunk rows x VS values (bf16, 128-byte swizzled rows).  Only the
-    // 64-row walks store this way: for 16 rows the stores measured slower (the
-    // 16K prefill's scan 204 against 182 us), for 64 faster (varlen batch 567
-    // against 582 us, mixed batch 63.5 against 65.9).
-    static constexpr int kOutBufs = NT >= 8 ? 2 : 0;
-    static constexpr int kOutBuf = 16 * VS * 2;
-    static constexpr int kOutWarpsN = 4;
-    static constexpr int kOut = round1k(kUt + kRing * kUtSlot);
-    static constexpr int kBar = kOut + kOutWarpsN * kOutBufs * kOutBuf;  // mbarriers (2 kStages + 2 kRing)
+    // The output rows are stored directly: staging them for TMA stores measured
+    // slower here (the 16K prefill's scan 204 against 182 us).
+    static constexpr int kBar = round1k(kUt + kRing * kUtSlot);  // mbarriers (2 kStages + 2 kRing)
     static constexpr int kAbort = kBar + 8 * (2 * kStages + 2 * kRing);  // int: a state warp gave up
     static constexpr int kTotal = kBar + 128;
     static_assert(kAbort + 4 <= kTotal, "mbarriers and the abort flag fit");
@@ -124,13 +118,9 @@ struct WalkRange {
     float* final_buf = nullptr;   // ... into this [128][128] fp32 plane instead of the pool
 };
 
-// out_map (64-row walks only): a tensor map of `out` ([T][H][128] bf16, box 64
-// values x 1 head x 16 rows, 128-byte swizzle) for TMA stores of whole chunks'
-// outputs, or nullptr (every output row stored directly).
 template <int NT>
 __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int n, int h, int z,
-                                          const WalkRange& R = WalkRange(),
-                                          const CUtensorMap* out_map = nullptr) {
+                                          const WalkRange& R = WalkRange()) {
     using L = ScanSmem<NT>;
     constexpr int VS = L::VS;
     constexpr int kStages = L::kStages;
@@ -239,7 +229,7 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
                 uint32_t a[4];
                 ldsm_x4(tqg + sw128_off(16 * wr + rr + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1), 64),
                         a[0], a[1], a[2], a[3]);
-                float (*d)[4] = (NT <= 4 && (ks & 1)) ? acc2 : acc;  // two chains for few n-tiles
+                float (*d)[4] = (ks & 1) ? acc2 : acc;  // two chains over the key halves
 #pragma unroll
                 for (int np = 0; np < NT / 2; ++np) {
                     uint32_t bb[4];
@@ -269,57 +259,21 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
                 mbar_arrive(&sfree[b]);
                 mbar_arrive(&empty[sg]);
             }
-            bool staged = false;
-            if constexpr (L::kOutBufs > 0) {
-                if (R.outputs && out_map && lc * C + C <= len) {
-                    // a whole chunk: the warp's 16 rows into its staging buffer
-                    // (bf16), then one TMA store; the buffer was last read
-                    // kOutBufs chunks back
-                    staged = true;
-                    const uint32_t ob =
-                        sm_base + L::kOut + (L::kOutBufs * wr + lc % L::kOutBufs) * L::kOutBuf;
-                    if (lane == 0) bulk_wait_read<L::kOutBufs - 1>();
-                    __syncwarp();
+            // each row of `out` directly (within the sequence)
 #pragma unroll
-                    for (int np = 0; np < NT / 2; ++np) {
-                        const int row = rr + 8 * (mi & 1), col = 16 * np + 8 * (mi >> 1);
-                        uint32_t pv[4];
+            for (int hh = 0; hh < 2; ++hh) {
+                const int i = 16 * wr + g + 8 * hh;
+                if (R.outputs && lc * C + i < len) {
+                    const size_t t = (size_t)(tok0 + lc * C + i);
+                    __nv_bfloat16* orow = p.out + (t * p.H + h) * D + v0;
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const int nt = 2 * np + (q4 >> 1), hh = q4 & 1;
-                            pv[q4] = pack_bf162(acc[nt][2 * hh] + acc2[nt][2 * hh],
-                                                acc[nt][2 * hh + 1] + acc2[nt][2 * hh + 1]);
-                        }
-                        stsm_x4(ob + sw64_off(row, col), pv[0], pv[1], pv[2], pv[3]);
-                    }
-                    fence_proxy_async();  // the staged rows are read by the TMA store
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_3d(out_map, smem + (ob - sm_base), v0, h, tok0 + lc * C + 16 * wr);
-                        bulk_commit();
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const uint32_t pv = pack_bf162(acc[nt][2 * hh] + acc2[nt][2 * hh],
+                                                       acc[nt][2 * hh + 1] + acc2[nt][2 * hh + 1]);
+                        *reinterpret_cast<uint32_t*>(orow + 8 * nt + 2 * tq) = pv;
                     }
                 }
             }
-            if (!staged) {  // each row of `out` directly (within the sequence)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int i = 16 * wr + g + 8 * hh;
-                    if (R.outputs && lc * C + i < len) {
-                        const size_t t = (size_t)(tok0 + lc * C + i);
-                        __nv_bfloat16* orow = p.out + (t * p.H + h) * D + v0;
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            const uint32_t pv = pack_bf162(acc[nt][2 * hh] + acc2[nt][2 * hh],
-                                                           acc[nt][2 * hh + 1] + acc2[nt][2 * hh + 1]);
-                            *reinterpret_cast<uint32_t*>(orow + 8 * nt + 2 * tq) = pv;
-                        }
-                    }
-                }
-            }
-        }
-        // the TMA stores have completed before the CTA's shared memory is released
-        if constexpr (L::kOutBufs > 0) {
-            if (lane == 0) bulk_wait_all();
         }
         return;
     }
@@ -384,23 +338,18 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
                           pack_half2(Sm[mt][2 * np + 1][2], Sm[mt][2 * np + 1][3]));
             }
     };
-    // B fragments of S for U = w S^T: [ks][nt][b0, b1]
     // S as the B operand of U = w S^T, [ks][nt][b0, b1]: loaded once after S is
-    // published for up to 32 value rows; with 64 the fragments are loaded per
-    // K step inside the product instead (they would take 128 registers)
-    constexpr bool kHoldS = NT <= 4;
-    uint32_t Sf[kHoldS ? 8 : 1][NT][2];
+    // published
+    uint32_t Sf[8][NT][2];
     auto load_sfrag = [&](int b) {
-        if constexpr (kHoldS) {
-            const uint32_t s16 = s16_slot(b);
+        const uint32_t s16 = s16_slot(b);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
+        for (int ks = 0; ks < 8; ++ks)
 #pragma unroll
-                for (int np = 0; np < NT / 2; ++np)
-                    ldsm_x4(s16 + sw128_off(16 * np + rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1), VS),
-                            Sf[ks][2 * np][0], Sf[ks][2 * np][1], Sf[ks][2 * np + 1][0],
-                            Sf[ks][2 * np + 1][1]);
-        }
+            for (int np = 0; np < NT / 2; ++np)
+                ldsm_x4(s16 + sw128_off(16 * np + rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1), VS),
+                        Sf[ks][2 * np][0], Sf[ks][2 * np][1], Sf[ks][2 * np + 1][0],
+                        Sf[ks][2 * np + 1][1]);
     };
 
     write_s16(0);
@@ -417,30 +366,16 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
         const uint32_t tu = st + L::kSharedPad;  // [VS/16][64][16] fp16
         const uint32_t ut = ut_slot(b);
 
-        // U = u - w S^T for chunk rows 16wr..16wr+15 (two chains over the key halves
-        // while there are few n-tiles)
-        constexpr int kUChains = NT <= 4 ? 2 : 1;
-        float accU[NT][4] = {}, accU2[kUChains == 2 ? NT : 1][4] = {};
+        // U = u - w S^T for chunk rows 16wr..16wr+15 (two chains over the key halves)
+        float accU[NT][4] = {}, accU2[NT][4] = {};
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             uint32_t a[4];
             ldsm_x4(tw + sw128_off(16 * wr + rr + 8 * (mi & 1), 16 * ks + 8 * (mi >> 1), 64), a[0],
                     a[1], a[2], a[3]);
-            if constexpr (kHoldS) {
-                float (*d)[4] = (kUChains == 2 && (ks & 1)) ? accU2 : accU;
+            float (*d)[4] = (ks & 1) ? accU2 : accU;
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma_f16(d[nt], a, Sf[ks][nt][0], Sf[ks][nt][1]);
-            } else {
-                const uint32_t s16 = s16_slot(b);
-#pragma unroll
-                for (int np = 0; np < NT / 2; ++np) {
-                    uint32_t sb4[4];
-                    ldsm_x4(s16 + sw128_off(16 * np + rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1), VS),
-                            sb4[0], sb4[1], sb4[2], sb4[3]);
-                    mma_f16(accU[2 * np], a, sb4[0], sb4[1]);
-                    mma_f16(accU[2 * np + 1], a, sb4[2], sb4[3]);
-                }
-            }
+            for (int nt = 0; nt < NT; ++nt) mma_f16(d[nt], a, Sf[ks][nt][0], Sf[ks][nt][1]);
         }
         uint32_t uf[NT][2];  // U as fp16 pairs: [nt][rows g, g + 8]
 #pragma unroll
@@ -455,11 +390,8 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
                              : "r"(tu + (vv >> 4) * kWsUSliceBytes + (i * 16 + (vv & 15)) * 2));
                 const float2 u2 = R.zero_u ? make_float2(0.f, 0.f)
                                            : __half22float2(*reinterpret_cast<__half2*>(&uv));
-                float x0 = u2.x - accU[nt][2 * hh], x1 = u2.y - accU[nt][2 * hh + 1];
-                if constexpr (kUChains == 2) {
-                    x0 -= accU2[nt][2 * hh];
-                    x1 -= accU2[nt][2 * hh + 1];
-                }
+                const float x0 = u2.x - accU[nt][2 * hh] - accU2[nt][2 * hh];
+                const float x1 = u2.y - accU[nt][2 * hh + 1] - accU2[nt][2 * hh + 1];
                 uf[nt][hh] = pack_half2(x0, x1);
             }
         // U^T into ring slot b (rows v, columns c): stmatrix transposes 8x8 blocks
@@ -471,50 +403,31 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
                       uf[2 * np + 1][1]);
         }
         // kg^T fragments of the update, loaded before the barrier (they do not
-        // depend on U) so that their latency overlaps the wait; for 64 value rows
-        // per K step of each half instead (registers)
-        auto load_kga = [&](int ks, int mt, uint32_t (&f)[4]) {
-            ldsm_x4_t(tkg + sw128_off(16 * ks + rr + 8 * (mi >> 1), 32 * wr + 16 * mt + 8 * (mi & 1), 64),
-                      f[0], f[1], f[2], f[3]);
-        };
-        constexpr bool kHoldKg = NT <= 4;
-        uint32_t kga[kHoldKg ? 4 : 1][2][4];
-        if constexpr (kHoldKg) {
+        // depend on U) so that their latency overlaps the wait
+        uint32_t kga[4][2][4];
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
+        for (int ks = 0; ks < 4; ++ks)
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt) load_kga(ks, mt, kga[ks][mt]);
-        }
+            for (int mt = 0; mt < 2; ++mt)
+                ldsm_x4_t(tkg + sw128_off(16 * ks + rr + 8 * (mi >> 1), 32 * wr + 16 * mt + 8 * (mi & 1), 64),
+                          kga[ks][mt][0], kga[ks][mt][1], kga[ks][mt][2], kga[ks][mt][3]);
         const int abort1 = state_sync_flag(!ok);  // a copy never landed (tested below)
         if (tid == 0) mbar_arrive(&sready[b]);  // S (published last step) and U of this chunk
 
-        // dS^T = kg^T U for key channels 32wr..32wr+31; S = gamma S + dS (for 64
-        // value rows in two halves of 32, which keeps the accumulators in registers)
-        constexpr int kVH = NT >= 8 ? 2 : 1, NTH = NT / kVH;
-#pragma unroll
-        for (int vh = 0; vh < kVH; ++vh) {
-            float accS[2][NTH][4] = {};
+        // dS^T = kg^T U for key channels 32wr..32wr+31; S = gamma S + dS
+        {
+            float accS[2][NT][4] = {};
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-                uint32_t bb[NTH][2];
+                uint32_t bb[NT][2];
 #pragma unroll
-                for (int np = 0; np < NTH / 2; ++np)
-                    ldsm_x4(ut + sw64_off(16 * (vh * NTH / 2 + np) + rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1)),
+                for (int np = 0; np < NT / 2; ++np)
+                    ldsm_x4(ut + sw64_off(16 * np + rr + 8 * (mi >> 1), 16 * ks + 8 * (mi & 1)),
                             bb[2 * np][0], bb[2 * np][1], bb[2 * np + 1][0], bb[2 * np + 1][1]);
-                uint32_t ka[2][4];
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    if constexpr (kHoldKg) {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) ka[mt][e] = kga[ks][mt][e];
-                    } else {
-                        load_kga(ks, mt, ka[mt]);
-                    }
-                }
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-                    for (int nt = 0; nt < NTH; ++nt) mma_f16(accS[mt][nt], ka[mt], bb[nt][0], bb[nt][1]);
+                    for (int nt = 0; nt < NT; ++nt) mma_f16(accS[mt][nt], kga[ks][mt], bb[nt][0], bb[nt][1]);
             }
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt)
@@ -522,10 +435,9 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
                 for (int hh = 0; hh < 2; ++hh) {
                     const float gk = gam[32 * wr + 16 * mt + g + 8 * hh];
 #pragma unroll
-                    for (int nt = 0; nt < NTH; ++nt) {
-                        const int n2 = vh * NTH + nt;
-                        Sm[mt][n2][2 * hh] = gk * Sm[mt][n2][2 * hh] + accS[mt][nt][2 * hh];
-                        Sm[mt][n2][2 * hh + 1] = gk * Sm[mt][n2][2 * hh + 1] + accS[mt][nt][2 * hh + 1];
+                    for (int nt = 0; nt < NT; ++nt) {
+                        Sm[mt][nt][2 * hh] = gk * Sm[mt][nt][2 * hh] + accS[mt][nt][2 * hh];
+                        Sm[mt][nt][2 * hh + 1] = gk * Sm[mt][nt][2 * hh + 1] + accS[mt][nt][2 * hh + 1];
                     }
                 }
         }

@@ -41,9 +41,8 @@ CASES = [
     ([8, 9, 1, 0, 7, 2, 64, 3], 2, torch.float32, 32),
     ([3] * 5 + [1] * 5 + [8], 3, torch.float16, 0),
     # more than 2 * SMs / 8 (sequence, head) pairs on a 152-SM GPU: the scan's
-    # large-batch form (64 value rows per CTA: S and kg fragments loaded per K
-    # step, the update in two halves, two stages), with one wave of CTAs and with
-    # more than one
+    # large-batch form, each warp owning 16 value rows of the state (64 value rows
+    # per CTA while those fit one wave, 128 beyond)
     ([70, 9, 128, 200, 65, 150, 33, 99, 64, 300] * 2, 2, torch.float32, 0),
     ([130, 65, 10, 257, 64] * 4, 2, torch.bfloat16, 64),
     ([70, 9, 128, 200, 65, 150, 33, 99, 64, 300] * 4, 2, torch.float32, 0),

@@ -35,8 +35,8 @@ int main() {
                     p.max_long_chunks = mc;
                     int L = 0;
                     const int P = kda::scan_segments(p, s, &L);
-                    std::printf("%d %d %d %d %d %d %d\n", s, nl, H, mc, P, L,
-                                kda::scan_groups(nl, H, s));
+                    std::printf("%d %d %d %d %d %d %d %d\n", s, nl, H, mc, P, L,
+                                kda::scan_groups(nl, H, s), kda::scan_groups(nl, H, s, s));
                 }
     return 0;
 }
@@ -70,7 +70,7 @@ def _seg_planes():
 def test_segment_plans_stay_inside_their_bounds(plans):
     planes = _seg_planes()
     taken = 0
-    for sms, nl, H, mc, P, L, _ in plans:
+    for sms, nl, H, mc, P, L, *_ in plans:
         if P == 0:
             continue
         taken += 1
@@ -84,15 +84,19 @@ def test_segment_plans_stay_inside_their_bounds(plans):
 
 
 def test_known_plans(plans):
-    by = {(s, nl, H, mc): (P, L) for s, nl, H, mc, P, L, _ in plans}
+    by = {(s, nl, H, mc): (P, L) for s, nl, H, mc, P, L, *_ in plans}
     assert by[(152, 1, 2, 256)] == (5, 52)    # 1 x 16384, H = 2: five segments of 52 chunks
     assert by[(152, 1, 6, 256)][0] == 0       # 6 pairs: the fused launch or the plain scan
     assert by[(152, 1, 1, 11)][0] == 0        # too short to cut
 
 
 def test_value_row_split(plans):
-    # 16 value rows per CTA while the walks of 16 fill at most two waves, else 64
-    for sms, nl, H, mc, P, L, groups in plans:
-        want = 1 if nl * H * 8 <= 2 * sms else 4
+    # 16 value rows per CTA while the walks of 16 fill at most two waves, 64 while
+    # the walks of 64 fit one wave, else 128; with a wave of token-by-token pairs
+    # beside the scan, 128 in place of 64
+    for sms, nl, H, mc, P, L, groups, groups_beside in plans:
+        pairs = nl * H
+        want = 1 if pairs * 8 <= 2 * sms else (4 if pairs * 2 <= sms else 8)
         assert groups == want, (sms, nl, H, groups)
-    assert any(g == 4 for *_, g in plans)
+        assert groups_beside == (1 if want == 1 else 8), (sms, nl, H, groups_beside)
+    assert any(g == 4 for *_, g, _ in plans) and any(g == 8 for *_, g, _ in plans)
