@@ -99,12 +99,29 @@ struct IntraMaps {
 };
 
 
-// Nearest tf32 value (ties away from zero) of x, as its fp32 bit pattern: add
-// half a tf32 unit in the last place to the magnitude bits and clear the 13 bits
-// below tf32 precision (a carry into the exponent is the correct rounding).
+// Nearest tf32 value (ties away from zero) of x, as its fp32 bit pattern (the
+// 13 bits below tf32 precision zero): one conversion instruction, which gives
+// the same bits as adding half a tf32 unit in the last place to the magnitude
+// and clearing those 13 bits (checked over 2^26 finite patterns on GB300).
 __device__ __forceinline__ uint32_t tf32_bits(float x) {
-    return (__float_as_uint(x) + 0x1000u) & 0xffffe000u;
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
 }
+__device__ __forceinline__ uint2 tf32_bits2(float2 x) { return make_uint2(tf32_bits(x.x), tf32_bits(x.y)); }
+
+// 2^x by the special-function unit (approximate; subnormal results flushed)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// Channel pairs: the decay pass holds two channels of a row as a float2 and
+// works on both with one packed fp32 instruction (sm_100 and later).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 splat2(float x) { return make_float2(x, x); }
+__device__ __forceinline__ uint32_t pack_half2v(float2 x) { return pack_half2(x.x, x.y); }
 
 // Marks a (chunk, head) block as written for the fused launch's scan walks: the
 // block's bulk stores have completed (cp.async.bulk.wait_group 0 by this
@@ -335,8 +352,9 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
             const int B = warp >> 2, hf = (warp >> 1) & 1;
             const int c0 = 64 * (warp & 1) + 2 * lane;
             const int rb = 16 * B + 8 * hf;
-            float a0[8], a1[8], q0[8], q1[8], k0[8], k1[8];
-            float L0 = 1.f, L1 = 1.f;
+            float2 a[8], q[8], k[8];  // the two channels' gate factors and (normed) q, k
+            float2 Lh = make_float2(1.f, 1.f);
+            const float2 m_log2e = splat2(-1.4426950408889634f), lb_log2e = splat2(lb * 1.4426950408889634f);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int r = rb + i;
@@ -350,24 +368,22 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
                 const bool valid = r < len;
                 // sigmoid of both channels from one reciprocal: with d = 1 + e^{-g}
                 // (g clamped to [-40, 40], where sigmoid is 0 or 1 to fp32 precision,
-                // so d0 d1 stays finite), s0 = d1 / (d0 d1) and s1 = d0 / (d0 d1)
-                const float d0 = 1.f + __expf(-fminf(fmaxf(gr.x, -40.f), 40.f));
-                const float d1 = 1.f + __expf(-fminf(fmaxf(gr.y, -40.f), 40.f));
-                const float rd = __fdividef(1.f, d0 * d1);
-                const float s0 = d1 * rd, s1 = d0 * rd;
-                a0[i] = valid ? __expf(lb * s0) : 1.f;
-                a1[i] = valid ? __expf(lb * s1) : 1.f;
-                L0 *= a0[i];
-                L1 *= a1[i];
+                // so d0 d1 stays finite), s0 = d1 / (d0 d1) and s1 = d0 / (d0 d1);
+                // e^x is taken as 2^(x log2 e)
+                const float2 t = mul2(make_float2(fminf(fmaxf(gr.x, -40.f), 40.f),
+                                                  fminf(fmaxf(gr.y, -40.f), 40.f)), m_log2e);
+                const float2 d = __fadd2_rn(make_float2(ex2_approx(t.x), ex2_approx(t.y)), splat2(1.f));
+                const float rd = __fdividef(1.f, d.x * d.y);
+                const float2 e = mul2(mul2(make_float2(d.y, d.x), splat2(rd)), lb_log2e);
+                a[i] = valid ? make_float2(ex2_approx(e.x), ex2_approx(e.y)) : make_float2(1.f, 1.f);
+                Lh = mul2(Lh, a[i]);
                 const uint32_t o16 = sw128_off(r, c0, 64);
                 const uint32_t qw = *reinterpret_cast<const uint32_t*>(smem + kQ + o16);
                 const uint32_t kw = *reinterpret_cast<const uint32_t*>(smem + kK + o16);
-                q0[i] = __uint_as_float(qw << 16);
-                q1[i] = __uint_as_float(qw & 0xffff0000u);
-                k0[i] = __uint_as_float(kw << 16);
-                k1[i] = __uint_as_float(kw & 0xffff0000u);
+                q[i] = make_float2(__uint_as_float(qw << 16), __uint_as_float(qw & 0xffff0000u));
+                k[i] = make_float2(__uint_as_float(kw << 16), __uint_as_float(kw & 0xffff0000u));
             }
-            *reinterpret_cast<float2*>(HT + (2 * B + hf) * 128 + c0) = make_float2(L0, L1);
+            *reinterpret_cast<float2*>(HT + (2 * B + hf) * 128 + c0) = Lh;
             {
                 // sums of squares of the 8 rows (value 2i: q, 2i + 1: k) over the
                 // warp's 64 channels: a halving butterfly leaves value lane / 2 in
@@ -375,8 +391,8 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
                 float x[16];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    x[2 * i] = fmaf(q0[i], q0[i], q1[i] * q1[i]);
-                    x[2 * i + 1] = fmaf(k0[i], k0[i], k1[i] * k1[i]);
+                    x[2 * i] = fmaf(q[i].x, q[i].x, q[i].y * q[i].y);
+                    x[2 * i + 1] = fmaf(k[i].x, k[i].x, k[i].y * k[i].y);
                 }
 #pragma unroll
                 for (int w = 8; w >= 1; w >>= 1) {  // lane bit 16, 8, 4, 2
@@ -416,10 +432,8 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
                 for (int i = 0; i < 8; ++i) {
                     const float sq = __shfl_sync(0xffffffffu, nf, 4 * i);
                     const float sk = __shfl_sync(0xffffffffu, nf, 4 * i + 2);
-                    q0[i] *= sq;
-                    q1[i] *= sq;
-                    k0[i] *= sk;
-                    k1[i] *= sk;
+                    q[i] = mul2(q[i], splat2(sq));
+                    k[i] = mul2(k[i], splat2(sk));
                 }
             }
             {
@@ -432,81 +446,65 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
                     uint4* vp = reinterpret_cast<uint4*>(smem + kV + sw128_off(r, c8, 64));
                     uint4 raw = *vp;
                     uint32_t* w4 = reinterpret_cast<uint32_t*>(&raw);
-                    const float br = beta[r];
+                    const float2 br = splat2(beta[r]);
 #pragma unroll
                     for (int x = 0; x < 4; ++x)
-                        w4[x] = pack_half2(br * __uint_as_float(w4[x] << 16),
-                                           br * __uint_as_float(w4[x] & 0xffff0000u));
+                        w4[x] = pack_half2v(mul2(br, make_float2(__uint_as_float(w4[x] << 16),
+                                                                __uint_as_float(w4[x] & 0xffff0000u))));
                     *vp = raw;
                 }
             }
             // block totals E_m = (first half) x (second half); F1 = product over
             // blocks before B, F2 = product over blocks after B
-            float E0[4], E1[4];
+            float2 E[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                E[m] = mul2(*reinterpret_cast<const float2*>(HT + (2 * m) * 128 + c0),
+                            *reinterpret_cast<const float2*>(HT + (2 * m + 1) * 128 + c0));
+            float2 f1 = make_float2(1.f, 1.f), f2 = make_float2(1.f, 1.f);
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-                const float2 t0 = *reinterpret_cast<const float2*>(HT + (2 * m) * 128 + c0);
-                const float2 t1 = *reinterpret_cast<const float2*>(HT + (2 * m + 1) * 128 + c0);
-                E0[m] = t0.x * t1.x;
-                E1[m] = t0.y * t1.y;
-            }
-            float f10 = 1.f, f11 = 1.f, f20 = 1.f, f21 = 1.f;
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                if (m < B) {
-                    f10 *= E0[m];
-                    f11 *= E1[m];
-                }
-                if (m > B) {
-                    f20 *= E0[m];
-                    f21 *= E1[m];
-                }
+                if (m < B) f1 = mul2(f1, E[m]);
+                if (m > B) f2 = mul2(f2, E[m]);
             }
             const float2 own0 = *reinterpret_cast<const float2*>(HT + (2 * B) * 128 + c0);
             const float2 own1 = *reinterpret_cast<const float2*>(HT + (2 * B + 1) * 128 + c0);
-            const float eb0 = own0.x * own1.x, eb1 = own0.y * own1.y;
+            const float2 eb = mul2(own0, own1);
             if (hf == 0) {
-                *reinterpret_cast<float2*>(F1 + B * 128 + c0) = make_float2(f10, f11);
+                *reinterpret_cast<float2*>(F1 + B * 128 + c0) = f1;
                 if (B == 1 || B == 2)
-                    *reinterpret_cast<uint32_t*>(MIDh + (B - 1) * 128 + c0) = pack_half2(eb0, eb1);
-                if (B == 0)
-                    *reinterpret_cast<float2*>(blk + kWsGammaOff + 4 * c0) =
-                        make_float2(eb0 * f20, eb1 * f21);
+                    *reinterpret_cast<uint32_t*>(MIDh + (B - 1) * 128 + c0) = pack_half2v(eb);
+                if (B == 0) *reinterpret_cast<float2*>(blk + kWsGammaOff + 4 * c0) = mul2(eb, f2);
             }
             // forward: P_i = (first-half product, for the second half) x prefix
-            float P0 = hf ? own0.x : 1.f, P1 = hf ? own0.y : 1.f;
+            float2 P = hf ? own0 : make_float2(1.f, 1.f);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int r = rb + i;
-                P0 *= a0[i];
-                P1 *= a1[i];
-                const float x0 = q0[i] * P0, x1 = q1[i] * P1;
-                const float l0 = k0[i] * P0, l1 = k1[i] * P1;
+                P = mul2(P, a[i]);
+                const float2 x = mul2(q[i], P), l = mul2(k[i], P);
                 const uint32_t o32 = sw128f_off(r, c0, 64);
-                *reinterpret_cast<uint2*>(smem + kLq32 + o32) = make_uint2(tf32_bits(x0), tf32_bits(x1));
-                *reinterpret_cast<uint2*>(smem + kLk32 + o32) = make_uint2(tf32_bits(l0), tf32_bits(l1));
+                *reinterpret_cast<uint2*>(smem + kLq32 + o32) = tf32_bits2(x);
+                *reinterpret_cast<uint2*>(smem + kLk32 + o32) = tf32_bits2(l);
                 if (B >= 1) {
                     const uint32_t h16 = sw128_off(r - 16, c0, 48);
-                    *reinterpret_cast<uint32_t*>(smem + kLQ + h16) = pack_half2(x0, x1);
-                    *reinterpret_cast<uint32_t*>(smem + kLK + h16) = pack_half2(l0, l1);
+                    *reinterpret_cast<uint32_t*>(smem + kLQ + h16) = pack_half2v(x);
+                    *reinterpret_cast<uint32_t*>(smem + kLK + h16) = pack_half2v(l);
                 }
-                *reinterpret_cast<uint32_t*>(blk + kWsQGOff + sw128_off(r, c0, 64)) =
-                    pack_half2(x0 * f10, x1 * f11);
+                *reinterpret_cast<uint32_t*>(blk + kWsQGOff + sw128_off(r, c0, 64)) = pack_half2v(mul2(x, f1));
             }
             // backward: R_i = product of a after row i in the block
-            const float ie0 = __fdividef(1.f, eb0), ie1 = __fdividef(1.f, eb1);
-            float R0 = hf ? 1.f : own1.x, R1 = hf ? 1.f : own1.y;
+            const float2 ie = make_float2(__fdividef(1.f, eb.x), __fdividef(1.f, eb.y));
+            float2 R = hf ? make_float2(1.f, 1.f) : own1;
 #pragma unroll
             for (int i = 7; i >= 0; --i) {
                 const int r = rb + i;
-                const float x0 = k0[i] * R0, x1 = k1[i] * R1;
-                *reinterpret_cast<uint2*>(smem + kRd32 + sw128f_off(r, c0, 64)) =
-                    make_uint2(tf32_bits(x0 * ie0), tf32_bits(x1 * ie1));
+                const float2 x = mul2(k[i], R);
+                *reinterpret_cast<uint2*>(smem + kRd32 + sw128f_off(r, c0, 64)) = tf32_bits2(mul2(x, ie));
                 const uint32_t o16 = sw128_off(r, c0, 64);
-                *reinterpret_cast<uint32_t*>(smem + kRO + o16) = pack_half2(x0, x1);
-                *reinterpret_cast<uint32_t*>(blk + kWsKGOff + o16) = pack_half2(x0 * f20, x1 * f21);
-                R0 *= a0[i];
-                R1 *= a1[i];
+                *reinterpret_cast<uint32_t*>(smem + kRO + o16) = pack_half2v(x);
+                *reinterpret_cast<uint32_t*>(blk + kWsKGOff + o16) = pack_half2v(mul2(x, f2));
+                R = mul2(R, a[i]);
             }
         }
         __syncthreads();
@@ -640,10 +638,10 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
                 const float4 kp = *reinterpret_cast<const float4*>(
                     smem + kLk32 + qt * 8192 + r * 128 + ((cc ^ (r & 7)) << 4));
                 const float4 f1 = *reinterpret_cast<const float4*>(F1 + (r >> 4) * 128 + c);
-                const float br = beta[r];
+                const float2 br = splat2(beta[r]);
                 *reinterpret_cast<uint2*>(smem + kX + sw128_off(r, c, 64)) =
-                    make_uint2(pack_half2(br * f1.x * kp.x, br * f1.y * kp.y),
-                               pack_half2(br * f1.z * kp.z, br * f1.w * kp.w));
+                    make_uint2(pack_half2v(mul2(mul2(br, make_float2(f1.x, f1.y)), make_float2(kp.x, kp.y))),
+                               pack_half2v(mul2(mul2(br, make_float2(f1.z, f1.w)), make_float2(kp.z, kp.w))));
             }
         }
         fence_proxy_async();  // the A_qk staging tile is read by the bulk store
