@@ -511,27 +511,30 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
         // q, k, g of this item are consumed: load the next item's now
         if (tid == kThreads - 32 && nxt < n_items) issue_inputs(nxt, tok_next);
 
-        // ---- A tiles: diagonal blocks (warps 0-7, tf32: block warp/2, q-left
-        //      or k-left) and off-diagonal block pairs (warps 8-13, fp16, q-left
-        //      and k-left sharing the right operand) --------------------------------
-        float acc[2][2][4] = {};
-        if (warp < 8) {
-            const int I = warp >> 1, which = warp & 1;  // which: 0 = q-left (A_qk), 1 = k-left
-            const uint32_t Lb = smem_u32(smem + (which ? kLk32 : kLq32));
+        // ---- A tiles: diagonal blocks (warps 0-3, tf32: block I = warp, A_qk and
+        //      A_kk sharing the right operand) and off-diagonal block pairs (warps
+        //      4-9, fp16, likewise) -------------------------------------------------
+        float acc[2][2][4] = {};  // [0]: q-left (A_qk), [1]: k-left (A_kk)
+        if (warp < 4) {
+            const int I = warp;
+            const uint32_t Lq = smem_u32(smem + kLq32), Lk = smem_u32(smem + kLk32);
             const uint32_t Rb = smem_u32(smem + kRd32);
 #pragma unroll 8
             for (int ks = 0; ks < 16; ++ks) {
-                uint32_t a4[4], b4[4];
-                ldsm_x4(Lb + sw128f_off(16 * I + rr + 8 * (mi & 1), 8 * ks + 4 * (mi >> 1), 64), a4[0],
-                        a4[1], a4[2], a4[3]);
+                uint32_t aq[4], ak[4], b4[4];
+                const uint32_t ao = sw128f_off(16 * I + rr + 8 * (mi & 1), 8 * ks + 4 * (mi >> 1), 64);
+                ldsm_x4(Lq + ao, aq[0], aq[1], aq[2], aq[3]);
+                ldsm_x4(Lk + ao, ak[0], ak[1], ak[2], ak[3]);
                 ldsm_x4(Rb + sw128f_off(16 * I + rr + 8 * (mi >> 1), 8 * ks + 4 * (mi & 1), 64), b4[0],
                         b4[1], b4[2], b4[3]);
-                mma_tf32(acc[0][0], a4, b4[0], b4[1]);
-                mma_tf32(acc[0][1], a4, b4[2], b4[3]);
+                mma_tf32(acc[0][0], aq, b4[0], b4[1]);
+                mma_tf32(acc[0][1], aq, b4[2], b4[3]);
+                mma_tf32(acc[1][0], ak, b4[0], b4[1]);
+                mma_tf32(acc[1][1], ak, b4[2], b4[3]);
             }
-        } else if (warp < 14) {
+        } else if (warp < 10) {
             int tI, tJ;
-            pair_of(warp - 8, tI, tJ);
+            pair_of(warp - 4, tI, tJ);
             // decay of the blocks strictly between J and I (blocks 1 and/or 2)
             const bool use1 = tJ < 1 && 1 < tI, use2 = tJ < 2 && 2 < tI;
             const uint32_t lq = smem_u32(smem + kLQ), lk = smem_u32(smem + kLK);
@@ -583,12 +586,13 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
                         ? load_raw(p.beta_raw, RAW16, (size_t)(tok_next + tid) * H + nxt % H)
                         : 0.f;
 
-        // ---- results into place; then the k-left diagonal warps invert their
-        //      16x16 block T_II = (I + A_II)^{-1} (registers, 16 lanes) ----------
-        if (warp < 8) {
-            const int I = warp >> 1;
-            put(warp & 1, I, I, acc[0]);
-            if (warp & 1) {
+        // ---- results into place; then the diagonal warps invert their 16x16
+        //      block T_II = (I + A_II)^{-1} (registers, 16 lanes) ------------------
+        if (warp < 4) {
+            const int I = warp;
+            put(0, I, I, acc[0]);
+            put(1, I, I, acc[1]);
+            {
                 __syncwarp();
                 if (lane < 16) {
                     // column col of T by forward substitution, column by column of
@@ -617,21 +621,19 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
                             __float2half_rn(t[i]);
                 }
             }
-        } else {
-            if (warp < 14) {
-                int tI, tJ;
-                pair_of(warp - 8, tI, tJ);
-                put(0, tI, tJ, acc[0]);
-                put(1, tI, tJ, acc[1]);
-            }
+        } else if (warp < 10) {
+            int tI, tJ;
+            pair_of(warp - 4, tI, tJ);
+            put(0, tI, tJ, acc[0]);
+            put(1, tI, tJ, acc[1]);
         }
         // ---- X = b k^ e^G in fp16 for the w product, by the 12 warps that do not
         //      invert (beside the 16x16 inverses): k^ P from its fp32 tile (a lane
         //      reads one 16-byte chunk, four columns, a warp two whole rows, so a
         //      read takes the four wavefronts 512 bytes need) times b and the
         //      prefix F1 of the row's block, into the free k^ E_B / P area
-        if (!(warp < 8 && (warp & 1))) {
-            const int xw = warp < 8 ? (warp >> 1) : warp - 4;  // 0..11
+        if (warp >= 4) {
+            const int xw = warp - 4;  // 0..11
             for (int pc = 32 * xw + lane; pc < 2048; pc += 12 * 32) {
                 const int r = pc >> 5, qt = (pc >> 3) & 3, cc = pc & 7;
                 const int c = 32 * qt + 4 * cc;
