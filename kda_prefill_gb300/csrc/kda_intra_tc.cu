@@ -633,17 +633,22 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
         //      read takes the four wavefronts 512 bytes need) times b and the
         //      prefix F1 of the row's block, into the free k^ E_B / P area
         if (warp >= 4) {
-            const int xw = warp - 4;  // 0..11
-            for (int pc = 32 * xw + lane; pc < 2048; pc += 12 * 32) {
-                const int r = pc >> 5, qt = (pc >> 3) & 3, cc = pc & 7;
-                const int c = 32 * qt + 4 * cc;
-                const float4 kp = *reinterpret_cast<const float4*>(
-                    smem + kLk32 + qt * 8192 + r * 128 + ((cc ^ (r & 7)) << 4));
-                const float4 f1 = *reinterpret_cast<const float4*>(F1 + (r >> 4) * 128 + c);
-                const float2 br = splat2(beta[r]);
-                *reinterpret_cast<uint2*>(smem + kX + sw128_off(r, c, 64)) =
-                    make_uint2(pack_half2v(mul2(mul2(br, make_float2(f1.x, f1.y)), make_float2(kp.x, kp.y))),
-                               pack_half2v(mul2(mul2(br, make_float2(f1.z, f1.w)), make_float2(kp.z, kp.w))));
+            // piece pc = row r (32 pieces of four columns each): lane = piece in
+            // the row, row r = warp - 4 + 12 j; a fixed trip count, so that the
+            // loads of all iterations can be in flight together
+            const int qt = lane >> 3, cc = lane & 7, c = 32 * qt + 4 * cc;
+#pragma unroll
+            for (int j = 0; j < 6; ++j) {
+                const int r = warp - 4 + 12 * j;
+                if (r < C) {
+                    const float4 kp = *reinterpret_cast<const float4*>(
+                        smem + kLk32 + qt * 8192 + r * 128 + ((cc ^ (r & 7)) << 4));
+                    const float4 f1 = *reinterpret_cast<const float4*>(F1 + (r >> 4) * 128 + c);
+                    const float2 br = splat2(beta[r]);
+                    *reinterpret_cast<uint2*>(smem + kX + sw128_off(r, c, 64)) = make_uint2(
+                        pack_half2v(mul2(mul2(br, make_float2(f1.x, f1.y)), make_float2(kp.x, kp.y))),
+                        pack_half2v(mul2(mul2(br, make_float2(f1.z, f1.w)), make_float2(kp.z, kp.w))));
+                }
             }
         }
         fence_proxy_async();  // the A_qk staging tile is read by the bulk store
