@@ -68,20 +68,11 @@ __device__ __forceinline__ void scan_walk_vp(const FwdParams& p, uint8_t* smem, 
     const int nch = p.seq_off[n + 1] - c0;
     const uint32_t sm_base = smem_u32(smem);
 
-    // this CTA's share of the shared part for the L2 prefetch (16-byte units)
-    constexpr int kGroups = D / L::VS;
-    constexpr int kUnits = kWsSharedBytes / 16;
-    const uint32_t pf_off = 16u * (uint32_t)(kUnits * z / kGroups);
-    const uint32_t pf_len = 16u * (uint32_t)(kUnits * (z + 1) / kGroups) - pf_off;
-    auto prefetch = [&](int lc) {
-        const uint8_t* src = p.ws + ((size_t)(c0 + lc) * p.H + h) * kWsBytes;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src + pf_off), "r"(pf_len)
-                     : "memory");
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
-                         src + kWsUOff + (v0 / 16) * kWsUSliceBytes),
-                     "r"((uint32_t)L::kU)
-                     : "memory");
-    };
+    // No L2 prefetch ahead of the stage copies: with a CTA per (sequence, head)
+    // on every SM, lines asked for several chunks ahead were evicted before
+    // their copy and read twice from DRAM (varlen batch: 2.48 GB read against
+    // the 1.57 GB of intermediates, scan 503 us; without the prefetch 415 us).
+
     // chunk lc's shared part and the CTA's u columns into stage lc % kStages
     auto issue_chunk = [&](int lc) {
         const int stage = lc % kStages;
@@ -106,14 +97,11 @@ __device__ __forceinline__ void scan_walk_vp(const FwdParams& p, uint8_t* smem, 
     if constexpr (NW >= 8) {
         // no producer warp: the first stages now, the others by the last warp done
         // with each stage (below)
-        if (tid == 0) {
-            for (int lc = 0; lc < kPrefetch && lc < nch; ++lc) prefetch(lc);
+        if (tid == 0)
             for (int lc = 0; lc < kStages && lc < nch; ++lc) issue_chunk(lc);
-        }
     } else if (warp == NW) {
         // ======================= producer warp ==============================
         if (lane == 0) {
-            for (int lc = 0; lc < kPrefetch && lc < nch; ++lc) prefetch(lc);
             int issued = 0;
             for (int lc = 0; lc < nch; ++lc) {
                 const int stage = lc % kStages;
@@ -121,7 +109,6 @@ __device__ __forceinline__ void scan_walk_vp(const FwdParams& p, uint8_t* smem, 
                     if (p.status) atomicOr(p.status, 1);
                     break;
                 }
-                if (lc + kPrefetch < nch) prefetch(lc + kPrefetch);
                 issue_chunk(lc);
                 issued = lc + 1;
             }
@@ -298,10 +285,7 @@ __device__ __forceinline__ void scan_walk_vp(const FwdParams& p, uint8_t* smem, 
                              : "memory");
                 if (old == NW - 1) {
                     done[sg] = 0;
-                    if (lc + kStages < nch) {
-                        if (lc + kStages + kPrefetch < nch) prefetch(lc + kStages + kPrefetch);
-                        issue_chunk(lc + kStages);
-                    }
+                    if (lc + kStages < nch) issue_chunk(lc + kStages);
                 }
             } else {
                 mbar_arrive(&empty[sg]);
