@@ -40,6 +40,9 @@ UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 126 << 20  # GB300 L2
+# GPU cycles spun before each call timed alone (~250 us at 2 GHz: longer than the
+# host's path through the binding for one call)
+HOST_LEAD_CYCLES = 500_000
 
 # Algorithmic bytes per token-head: q, k, v (bf16, 256 B each), raw gate
 # (fp32, 512 B), raw beta (4 B) read, and out (bf16, 256 B) written.
@@ -279,6 +282,10 @@ def time_calls(fn, steps, stream, flush_buf=None):
               for _ in range(steps)]
         for a, z in ev:
             flush_buf.zero_()
+            # the GPU spins (outside the events) while the host enqueues the
+            # call, so that the events time the call's kernels rather than the
+            # host's path through the binding
+            torch.cuda._sleep(HOST_LEAD_CYCLES)
             a.record(stream)
             fn()
             z.record(stream)
@@ -390,24 +397,9 @@ def run_ours(args, rank, world):
         """Milliseconds of args.steps calls of fn, CUDA events on the launching
         stream; with the flush, each call is timed alone after an L2 flush."""
         barrier()
-        if flush:
-            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(args.steps)]
-            for a, z in ev:
-                scratch.zero_()
-                a.record(stream)
-                fn()
-                z.record(stream)
-            barrier()
-            return sum(a.elapsed_time(z) for a, z in ev)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            fn()
-        e1.record(stream)
+        ms = time_calls(fn, args.steps, stream, scratch)
         barrier()
-        return e0.elapsed_time(e1)
+        return ms
 
     ms_total = time_steps(step)
     # keep the GPU busy with the same step until the clock sampling spans
