@@ -47,6 +47,11 @@ CASES = [
     ([130, 65, 10, 257, 64] * 4, 2, torch.bfloat16, 64),
     ([70, 9, 128, 200, 65, 150, 33, 99, 64, 300] * 4, 2, torch.float32, 0),
     ([130, 65, 10, 257, 64] * 8, 2, torch.bfloat16, 64),
+    # 64 value rows per CTA with a few token-by-token pairs beside the scan (fp16
+    # pool, padded slot stride); 128 rows chosen because a wave of token-by-token
+    # pairs runs beside a scan whose 64-row walks would fit one wave
+    ([130, 65, 257] * 7 + [1] * 10, 2, torch.float16, 128),
+    ([100] * 30 + [1] * 80, 2, torch.bfloat16, 0),
     # many short sequences: each persistent token-by-token CTA takes several items,
     # so its ring of state stages wraps around more than once
     ([1] * 300 + [2, 0, 5, 8] * 20, 2, torch.bfloat16, 0),
