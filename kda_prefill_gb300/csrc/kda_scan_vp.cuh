@@ -11,10 +11,12 @@
 // rows are the MMAs' M dimension.)  An m16n8 accumulator pair is an m16k16 A
 // fragment, so no product needs another warp's rows or a shared-memory round
 // trip of S or U: the warps never synchronise with each other.  Each warp reads
-// the chunk's w, qg, kg and A_qk tiles itself (the B operands), which the 16-row
-// walks (kda_scan_walk.cuh) spread over eight warps; at 64 value rows per CTA that
-// trade took the varlen batch's scan from 566 to 495 us.  The output rows are staged (stmatrix,
-// transposing) and stored with one TMA store per warp and chunk.
+// the chunk's w, qg, kg and A_qk tiles itself (the B operands), which the
+// role-split walk (kda_scan_walk.cuh) spreads over eight warps at the price of
+// moving S and U through shared memory twice per chunk; at 64 value rows per CTA
+// this form took the varlen batch's scan from 566 to 495 us.  The output rows
+// are staged (stmatrix, transposing) and stored with one TMA store per warp and
+// chunk.
 #pragma once
 
 #include "kda_scan_walk.cuh"
