@@ -156,7 +156,10 @@ unsigned launched_kernels(const FwdParams& p);
 
 // Individual stages (kda_intra.cu, kda_scan.cu, kda_decode.cu).
 cudaError_t launch_intra(const FwdParams& p, cudaStream_t s);
-cudaError_t launch_scan(const FwdParams& p, int groups, cudaStream_t s);
+// after_intra: launched right behind the intra-chunk kernel with programmatic
+// stream serialization, so that its CTAs take SMs as that kernel's CTAs finish;
+// the walks read the intermediates only once it has completed.
+cudaError_t launch_scan(const FwdParams& p, int groups, cudaStream_t s, bool after_intra = false);
 // beside_scan: launched right after the scan with programmatic stream
 // serialization, so that its CTAs take the SMs the scan's walks leave free (the
 // decode's items are other sequences, independent of the scan's); the decode

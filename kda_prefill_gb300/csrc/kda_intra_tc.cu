@@ -753,6 +753,10 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
 template <bool RAW16>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
+    // the scan launched after this grid may place its CTAs on the SMs this
+    // grid's CTAs leave when their items are done (it waits for the whole grid
+    // before it reads the intermediates)
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (call_aborted(p)) return;
     extern __shared__ __align__(1024) uint8_t smem[];
     StaticClaims cl;

@@ -53,7 +53,9 @@ cudaError_t launch_forward(const FwdParams& p, cudaStream_t s, cudaEvent_t* mark
     }
     if (marks) cudaEventRecord(marks[1], s);
     if (!fused) {
-        e = launch_scan(q, groups_of(q), s);
+        // right behind the intra-chunk kernel (not when the kernels are timed
+        // one by one)
+        e = launch_scan(q, groups_of(q), s, !marks && q.n_chunks > 0);
         if (e != cudaSuccess) return e;
     }
     if (marks) cudaEventRecord(marks[2], s);

@@ -237,8 +237,27 @@ cudaError_t launch_scan_segmented(const FwdParams& p, int P, int L, cudaStream_t
     return cudaGetLastError();
 }
 
+// Kernel launch, with programmatic stream serialization when `pdl` is set (the
+// grid may then start beside the kernel launched before it and waits for that
+// kernel's completion inside the walks, before it reads the intermediates).
+template <typename... Params, typename... Args>
+cudaError_t launch_maybe_pdl(void (*kernel)(Params...), unsigned grid, unsigned block, size_t smem,
+                             cudaStream_t s, bool pdl, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <int NT>
-cudaError_t launch_scan_nt(const FwdParams& p, cudaStream_t s) {
+cudaError_t launch_scan_nt(const FwdParams& p, cudaStream_t s, bool pdl) {
     using L = scan::ScanSmem<NT>;
     static unsigned configured = 0;
     int dev = 0;
@@ -253,8 +272,8 @@ cudaError_t launch_scan_nt(const FwdParams& p, cudaStream_t s) {
     const int n_seq = p.long_list ? p.n_long : p.N;
     if (n_seq <= 0) return cudaSuccess;
     const long blocks = (long)n_seq * p.H * (kD / L::VS);
-    kda_scan_mma<NT><<<(unsigned)blocks, scan::kScanThreads, L::kTotal, s>>>(p);
-    return cudaGetLastError();
+    return launch_maybe_pdl(kda_scan_mma<NT>, (unsigned)blocks, scan::kScanThreads, L::kTotal, s, pdl,
+                            p);
 }
 
 // One CTA per (long sequence, head, 16 NW value rows), sequence-major like
@@ -273,7 +292,7 @@ kda_scan_vp(FwdParams p, const __grid_constant__ CUtensorMap out_map, int has_ou
 }
 
 template <int NW>
-cudaError_t launch_scan_vp(const FwdParams& p, cudaStream_t s) {
+cudaError_t launch_scan_vp(const FwdParams& p, cudaStream_t s, bool pdl) {
     using L = scan::ScanSmemVP<NW>;
     static unsigned configured = 0;
     int dev = 0;
@@ -290,9 +309,8 @@ cudaError_t launch_scan_vp(const FwdParams& p, cudaStream_t s) {
     const long blocks = (long)n_seq * p.H * (kD / L::VS);
     CUtensorMap out_map = {};
     const int has_out_map = make_out_map(&out_map, p, 16, kC) ? 1 : 0;
-    kda_scan_vp<NW><<<(unsigned)blocks, scan::vp_threads<NW>(), L::kTotal, s>>>(p, out_map,
-                                                                               has_out_map);
-    return cudaGetLastError();
+    return launch_maybe_pdl(kda_scan_vp<NW>, (unsigned)blocks, scan::vp_threads<NW>(), L::kTotal, s,
+                            pdl, p, out_map, has_out_map);
 }
 
 }  // namespace
@@ -327,13 +345,13 @@ int scan_segments(const FwdParams& p, int num_sms, int* L) {
     return (p.max_long_chunks + *L - 1) / *L;
 }
 
-cudaError_t launch_scan(const FwdParams& p, int groups, cudaStream_t s) {
+cudaError_t launch_scan(const FwdParams& p, int groups, cudaStream_t s, bool after_intra) {
     if (p.N <= 0) return cudaSuccess;
     int L = 0;
     const int P = scan_segments(p, num_sms(), &L);
     if (P > 0) return launch_scan_segmented(p, P, L, s);
-    if (groups <= 1) return launch_scan_nt<2>(p, s);
-    return groups == 4 ? launch_scan_vp<4>(p, s) : launch_scan_vp<8>(p, s);
+    if (groups <= 1) return launch_scan_nt<2>(p, s, after_intra);
+    return groups == 4 ? launch_scan_vp<4>(p, s, after_intra) : launch_scan_vp<8>(p, s, after_intra);
 }
 
 }  // namespace kda

@@ -99,11 +99,16 @@ __device__ __forceinline__ void scan_walk_vp(const FwdParams& p, uint8_t* smem, 
     if constexpr (NW >= 8) {
         // no producer warp: the first stages now, the others by the last warp done
         // with each stage (below)
-        if (tid == 0)
+        // launched right behind the intra-chunk kernel, the CTA may start while
+        // that kernel's last items run: the intermediates are read after it is done
+        if (tid == 0) {
+            grid_dep_wait();
             for (int lc = 0; lc < kStages && lc < nch; ++lc) issue_chunk(lc);
+        }
     } else if (warp == NW) {
         // ======================= producer warp ==============================
         if (lane == 0) {
+            grid_dep_wait();  // the intermediates are read after the intra-chunk kernel
             int issued = 0;
             for (int lc = 0; lc < nch; ++lc) {
                 const int stage = lc % kStages;
@@ -158,6 +163,7 @@ __device__ __forceinline__ void scan_walk_vp(const FwdParams& p, uint8_t* smem, 
                     b[2 * np][0], b[2 * np][1], b[2 * np + 1][0], b[2 * np + 1][1]);
     };
 
+    grid_dep_wait();  // the state came from the pool; the chunks come after
     bool failed = false;
     for (int lc = 0; lc < nch; ++lc) {
         const int sg = lc % kStages;

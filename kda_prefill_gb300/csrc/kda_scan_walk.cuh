@@ -162,7 +162,10 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
     asm volatile("bar.sync 2, %0;" ::"n"(kScanThreads) : "memory");
 
     // ======================= producer warp ==================================
+    // Launched right behind the intra-chunk kernel, the CTA may start while that
+    // kernel's last items run: the intermediates are read only after it is done.
     if (warp == kStateWarps + kOutWarps) {
+        grid_dep_wait();
         if (lane == 0) {
             // this CTA's share of the shared part for the L2 prefetch (16-byte units)
             constexpr int kGroups = D / VS;
@@ -211,6 +214,7 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
 
     // ======================= output warps ===================================
     if (warp >= kStateWarps) {
+        grid_dep_wait();
         const int wr = warp - kStateWarps;  // chunk rows 16wr..16wr+15
         for (int lc = 0; lc < nch; ++lc) {
             const int b = lc % kRing, sg = lc % kStages;
@@ -352,6 +356,7 @@ __device__ __forceinline__ void scan_walk(const FwdParams& p, uint8_t* smem, int
                         Sf[ks][2 * np + 1][1]);
     };
 
+    grid_dep_wait();  // the state came from the pool; the chunks come after
     write_s16(0);
     state_sync();
     load_sfrag(0);
