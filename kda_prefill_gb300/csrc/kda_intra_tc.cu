@@ -632,6 +632,16 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
         //      reads one 16-byte chunk, four columns, a warp two whole rows, so a
         //      read takes the four wavefronts 512 bytes need) times b and the
         //      prefix F1 of the row's block, into the free k^ E_B / P area
+        // the A_qk blocks above the diagonal are zero, so that the tile, which goes
+        // out whole, is the full lower-triangular matrix and holds no stale shared
+        // memory; warps 10..15 take one block each: (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+        if (warp >= 10) {
+            const int b = warp - 10;
+            const int I = b < 3 ? 0 : (b < 5 ? 1 : 2);
+            const int J = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
+            *reinterpret_cast<uint4*>(smem + kAqkStage + sw64_off(16 * I + (lane >> 1), 16 * J + 8 * (lane & 1))) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
         if (warp >= 4) {
             // piece pc = row r (32 pieces of four columns each): lane = piece in
             // the row, row r = warp - 4 + 12 j; a fixed trip count, so that the
