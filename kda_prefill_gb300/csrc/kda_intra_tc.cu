@@ -28,10 +28,11 @@
 // channels; the halves exchange their products, and the rows' sums of squares
 // (for the norms) are reduced in-warp and exchanged at the same barrier.
 //
-// The solve is a blocked forward substitution on the right-hand sides:
-// W_I = T_II (X_I - sum_{J<I} A_IJ W_J) with the 16x16 inverses T_II computed in
-// registers; each warp owns 16 of the 256 columns of [X | Y] and works in
-// transposed form, so that every intermediate stays an MMA fragment.
+// The solve forms T = (I + A_kk)^{-1} in full: the 16x16 inverses T_II by
+// forward substitution in registers (one warp per block), then the blocks below
+// the diagonal column by column, T_IJ = T_II sum_{J<=m<I} (-A_Im) T_mJ, by three
+// warps while the others form X = b k^ e^G; [w | u] = T [X | b v] is then one
+// K = 64 product on the tensor cores (tcgen05, accumulators in tensor memory).
 //
 // Data movement: inputs by TMA tiled loads (3-D tensor maps over [T][H][128],
 // 128-byte swizzle); the next item's q, k, g are loaded as soon as the decay
@@ -204,6 +205,19 @@ __device__ __forceinline__ void t_column(uint8_t* smem, int lane) {
         *reinterpret_cast<uint4*>(smem + kT16 + sw64_off(16 * J + (lane >> 1), 16 * I + 8 * (lane & 1))) =
             make_uint4(0u, 0u, 0u, 0u);
     }
+}
+
+// Hand-off of the solve's blocks from the warps that put or invert them (warps
+// 3..9 arrive) to the warps that form T's block columns (warps 0..2 wait), on
+// named barrier 1, so that T is formed while the other warps form X.  An arrive
+// orders the arriving warp's earlier shared stores before the waiters' later
+// loads, as a CTA barrier does.
+constexpr int kSolveBarThreads = 320;
+__device__ __forceinline__ void solve_bar_wait() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kSolveBarThreads) : "memory");
+}
+__device__ __forceinline__ void solve_bar_arrive() {
+    asm volatile("bar.arrive 1, %0;" ::"n"(kSolveBarThreads) : "memory");
 }
 
 // The intra-chunk items of one CTA, in the order `cl` hands them out (all
@@ -587,7 +601,8 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
                         : 0.f;
 
         // ---- results into place; then the diagonal warps invert their 16x16
-        //      block T_II = (I + A_II)^{-1} (registers, 16 lanes) ------------------
+        //      block T_II = (I + A_II)^{-1} (registers, 16 lanes) and warps 0..2
+        //      form T's block columns, beside the X rows --------------------------
         if (warp < 4) {
             const int I = warp;
             put(0, I, I, acc[0]);
@@ -621,11 +636,26 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
                             __float2half_rn(t[i]);
                 }
             }
+            // ---- T = (I + A_kk)^{-1} in full, once every T_II and -A_Im is in
+            //      place: warp J forms block column J below the diagonal,
+            //      T_IJ = T_II sum_{J<=m<I} (-A_Im) T_mJ for I = J+1..3, in
+            //      transposed form (T_IJ^T = (sum T_mJ^T (-A_Im)^T) T_II^T) so that
+            //      each result is already the A fragment of the next product, and
+            //      zeroes the blocks above the diagonal in row J (t_column)
+            if (warp < 3) {
+                solve_bar_wait();
+                if (warp == 0) t_column<0>(smem, lane);
+                if (warp == 1) t_column<1>(smem, lane);
+                if (warp == 2) t_column<2>(smem, lane);
+            } else {
+                solve_bar_arrive();
+            }
         } else if (warp < 10) {
             int tI, tJ;
             pair_of(warp - 4, tI, tJ);
             put(0, tI, tJ, acc[0]);
             put(1, tI, tJ, acc[1]);
+            solve_bar_arrive();
         }
         // ---- X = b k^ e^G in fp16 for the w product, by the 12 warps that do not
         //      invert (beside the 16x16 inverses): k^ P from its fp32 tile (a lane
@@ -661,25 +691,14 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
                 }
             }
         }
-        fence_proxy_async();  // the A_qk staging tile is read by the bulk store
+        // the A_qk staging tile is read by the bulk store, T's blocks and X by the
+        // tensor cores
+        fence_proxy_async();
         __syncthreads();
         if (tid == 0) {
             bulk_s2g(blk + kWsAqkOff, smem + kAqkStage, 8192);
             bulk_commit();
         }
-
-        // ---- T = (I + A_kk)^{-1} in full: warp J forms block column J below the
-        //      diagonal, T_IJ = T_II sum_{J<=m<I} (-A_Im) T_mJ for I = J+1..3, in
-        //      transposed form (T_IJ^T = (sum T_mJ^T (-A_Im)^T) T_II^T) so that
-        //      each result is already the A fragment of the next product, and
-        //      zeroes the blocks above the diagonal in row J (t_column).
-        if (warp < 3) {
-            if (warp == 0) t_column<0>(smem, lane);
-            if (warp == 1) t_column<1>(smem, lane);
-            if (warp == 2) t_column<2>(smem, lane);
-            fence_proxy_async();  // T's blocks (generic stores) are read by the tensor cores
-        }
-        __syncthreads();
 
         // ---- [w | u] = T [X | Y] on the tensor cores: A = T (K-major), B = X and
         //      Y read MN-major from their row-major tiles (K = the chunk's rows)
