@@ -213,6 +213,7 @@ __device__ __forceinline__ void t_column(uint8_t* smem, int lane) {
 // orders the arriving warp's earlier shared stores before the waiters' later
 // loads, as a CTA barrier does.
 constexpr int kSolveBarThreads = 320;
+constexpr int kStoreTid = kThreads - 32;  // issues the bulk stores (lane 0 of warp 15)
 __device__ __forceinline__ void solve_bar_wait() {
     asm volatile("bar.sync 1, %0;" ::"n"(kSolveBarThreads) : "memory");
 }
@@ -356,8 +357,8 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
         //      c0 + 1) over 8 rows.  Part 1: a = e^{lb sigmoid(g)}, the half's
         //      product, q and k kept in registers, and the rows' sums of squares
         //      over the warp's 64 channels; the halves exchange their products
-        //      and the two warps of a row their sums.  Part 2: row norms, b v (two
-        //      16-byte pieces per thread), forward P (q^ P and k^ P: tf32 for the
+        //      and the two warps of a row their sums.  Part 2: row norms,
+        //      forward P (q^ P and k^ P: tf32 for the
         //      diagonal tiles, fp16 for the off-diagonal left operands, qg =
         //      q^ e^G to the workspace), backward R = product of a after the row
         //      in the block (k^ R / E_B in tf32, k^ R in fp16, kg = k^ e^{G_C - G}
@@ -424,16 +425,9 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
             if (tid < C) beta[tid] = (tid < len) ? __fdividef(1.f, 1.f + __expf(-braw)) : 0.f;
             // the previous item's bulk stores must have read the staging areas
             // (u in the q^P area, A_qk in the k^/P area, w in the LQ area) before
-            // part 2 rewrites them; for the fused launch they must have completed,
-            // and the item is then marked written
-            if (tid == 0) {
-                if (p.ready && prev >= 0) {
-                    bulk_wait_all();
-                    publish_ready(p.ready + prev);
-                } else {
-                    bulk_wait_read_all();
-                }
-            }
+            // part 2 rewrites them (their completion, for the fused launch's ready
+            // flag, is awaited during the tiles, off the CTA's barriers)
+            if (tid == kStoreTid) bulk_wait_read_all();
             __syncthreads();
             {
                 // row norms: lane 2v (v = 2i + s) forms the norm factor of value v
@@ -448,24 +442,6 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
                     const float sk = __shfl_sync(0xffffffffu, nf, 4 * i + 2);
                     q[i] = mul2(q[i], splat2(sq));
                     k[i] = mul2(k[i], splat2(sk));
-                }
-            }
-            {
-                const bool ok_v = mbar_wait(&bar[1], n_local & 1);
-                if (!ok_v && p.status) atomicOr(p.status, 1);
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {  // 16-byte pieces of v: 64 rows x 16
-                    const int pc = tid + kThreads * e;
-                    const int r = pc >> 4, c8 = (pc & 15) * 8;
-                    uint4* vp = reinterpret_cast<uint4*>(smem + kV + sw128_off(r, c8, 64));
-                    uint4 raw = *vp;
-                    uint32_t* w4 = reinterpret_cast<uint32_t*>(&raw);
-                    const float2 br = splat2(beta[r]);
-#pragma unroll
-                    for (int x = 0; x < 4; ++x)
-                        w4[x] = pack_half2v(mul2(br, make_float2(__uint_as_float(w4[x] << 16),
-                                                                __uint_as_float(w4[x] & 0xffff0000u))));
-                    *vp = raw;
                 }
             }
             // block totals E_m = (first half) x (second half); F1 = product over
@@ -526,8 +502,9 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
         if (tid == kThreads - 32 && nxt < n_items) issue_inputs(nxt, tok_next);
 
         // ---- A tiles: diagonal blocks (warps 0-3, tf32: block I = warp, A_qk and
-        //      A_kk sharing the right operand) and off-diagonal block pairs (warps
-        //      4-9, fp16, likewise) -------------------------------------------------
+        //      A_kk sharing the right operand), off-diagonal block pairs (warps
+        //      4-9, fp16, likewise), b v (warps 10-14) and the previous item's
+        //      ready flag (warp 15) ----------------------------------------------
         float acc[2][2][4] = {};  // [0]: q-left (A_qk), [1]: k-left (A_kk)
         if (warp < 4) {
             const int I = warp;
@@ -590,6 +567,35 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
                 mma_f16(acc[0][1], aq, b4[2], b4[3]);
                 mma_f16(acc[1][0], ak, b4[0], b4[1]);
                 mma_f16(acc[1][1], ak, b4[2], b4[3]);
+            }
+        } else if (warp == 15) {
+            // the thread that issued the previous item's bulk stores waits for
+            // them to complete and marks that item written (fused launch)
+            if (lane == 0 && p.ready && prev >= 0) {
+                bulk_wait_all();
+                publish_ready(p.ready + prev);
+            }
+        } else {
+            // warps 10..14, free during the tiles: b v in fp16, in place (the right
+            // operand of the u product), 16-byte pieces of v (64 rows x 16)
+            const bool ok_v = mbar_wait(&bar[1], n_local & 1);
+            if (!ok_v && p.status) atomicOr(p.status, 1);
+            constexpr int kBvThreads = kThreads - 320 - 32;
+#pragma unroll
+            for (int e = 0; e < (C * 16 + kBvThreads - 1) / kBvThreads; ++e) {
+                const int pc = tid - 320 + kBvThreads * e;
+                if (pc < C * 16) {
+                    const int r = pc >> 4, c8 = (pc & 15) * 8;
+                    uint4* vp = reinterpret_cast<uint4*>(smem + kV + sw128_off(r, c8, 64));
+                    uint4 raw = *vp;
+                    uint32_t* w4 = reinterpret_cast<uint32_t*>(&raw);
+                    const float2 br = splat2(beta[r]);
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+                        w4[x] = pack_half2v(mul2(br, make_float2(__uint_as_float(w4[x] << 16),
+                                                                __uint_as_float(w4[x] & 0xffff0000u))));
+                    *vp = raw;
+                }
             }
         }
         __syncthreads();  // the operand tiles are consumed (k^ P stays for the solve)
@@ -695,7 +701,7 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
         // tensor cores
         fence_proxy_async();
         __syncthreads();
-        if (tid == 0) {
+        if (tid == kStoreTid) {
             bulk_s2g(blk + kWsAqkOff, smem + kAqkStage, 8192);
             bulk_commit();
         }
@@ -759,7 +765,7 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
         tc_fence_before();
         fence_proxy_async();
         __syncthreads();
-        if (tid == 0) {
+        if (tid == kStoreTid) {
             bulk_s2g(blk + kWsWOff, smem + kLQ, 16384);
             bulk_s2g(blk + kWsUOff, smem + kLq32, 16384);
             bulk_commit();
@@ -768,7 +774,7 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
         prev = it;
         it = nxt;
     }
-    if (tid == 0) {
+    if (tid == kStoreTid) {
         bulk_wait_all();  // stores complete before the CTA releases its smem
         if (p.ready && prev >= 0) publish_ready(p.ready + prev);
     }
