@@ -891,10 +891,14 @@ bool make_maps(IntraMaps* maps, const FwdParams& p) {
 
 // SMs kept on intra-chunk items once the walks have started, at least.
 constexpr int kFusedIntraSms = 32;
-// How many intra items one SM finishes while a walk advances by one chunk: a
-// walk step takes ~0.68 us and an item ~7.5 us on GB300 (ratio 0.09); 0.085 was
-// the fastest of 0.07 .. 0.125 on the 1 x 4096 and 1 x 16384, H = 12 prefills.
-constexpr double kItemsPerWalkStep = 0.085;
+// How many intra items one SM finishes while a walk advances by one chunk (a
+// walk step takes ~0.7 us and an item ~7.3 us on GB300), and a lead of whole
+// walk steps' items done before the walks start (a CTA that claims a walk first
+// finishes its item).  Fitted on the 1 x 4096 and 1 x 16384, H = 12 prefills:
+// with the lead, 0.11 puts the split where each was fastest in a sweep of
+// 0.065 .. 0.16 without it (about 450 of 768 and 1570 of 3072 items).
+constexpr double kItemsPerWalkStep = 0.11;
+constexpr int kWalkLeadSteps = 6;
 
 // Per device: cooperative launch supported and one fused CTA fits on an SM.
 int g_fused_state[32] = {0};  // per device: 0 unknown, 1 usable, 2 not
@@ -955,10 +959,11 @@ cudaError_t launch_fused(const FwdParams& p, cudaStream_t s) {
     // Split: the walks start once the items done before them, plus what the
     // remaining SMs finish meanwhile, keep each walk's next chunk ready: per
     // chunk step the walks consume `pairs` items and the other SMs produce
-    // (sms - n_walks) * kItemsPerWalkStep.
+    // (sms - n_walks) * kItemsPerWalkStep; the first chunk's items and a lead
+    // of kWalkLeadSteps steps are done before.
     const double steps = (double)p.n_chunks / n_seq;  // chunks per sequence, on average
     const double deficit = pairs - (sms - n_walks) * kItemsPerWalkStep;
-    double split = pairs + (steps - 1.0) * (deficit > 0 ? deficit : 0.0);
+    double split = (double)pairs * (1 + kWalkLeadSteps) + (steps - 1.0) * (deficit > 0 ? deficit : 0.0);
     if (split > n_items) split = n_items;
     // (the work counter is cleared with the status word by the caller)
     cudaError_t e = cudaMemsetAsync(p.ready, 0, (size_t)n_items * sizeof(int), s);
