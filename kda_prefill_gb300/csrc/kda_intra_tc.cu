@@ -233,8 +233,9 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
     float* F1 = NS + 256;   // [4][128] decay of the blocks before B (e^G at the block start)
     float* HT = F1 + 512;   // [4][2][128] decay product of each 8-row half block
     __half* MIDh = reinterpret_cast<__half*>(smem + kMid);     // [2][128] E_1, E_2 in fp16
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBar);  // [0] q,k,g  [1] v  [2] w/u MMA
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBar);  // [0] q,k,g  [1] v  [2] w MMA
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kBar + 24);  // tensor-memory base
+    uint64_t* bar_u = reinterpret_cast<uint64_t*>(smem + kBar + 40);  // u MMA
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -252,6 +253,7 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
         mbar_init(&bar[2], 1);
+        mbar_init(bar_u, 1);
         fence_mbar_init();
         prefetch_tmap(&maps.q);
         prefetch_tmap(&maps.k);
@@ -707,54 +709,56 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
         }
 
         // ---- [w | u] = T [X | Y] on the tensor cores: A = T (K-major), B = X and
-        //      Y read MN-major from their row-major tiles (K = the chunk's rows)
+        //      Y read MN-major from their row-major tiles (K = the chunk's rows);
+        //      w and u complete on mbarriers of their own, so that w is read back
+        //      while the u product runs
         if (tid == 0) {
             tc_fence_after();
             const uint32_t sb = smem_u32(smem);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {  // K = 16 rows per MMA
-                const uint64_t a = sw128_desc(sb + kT16 + ks * 32, 16, 1024);
-                mma_f16_ss(tmem, a, sw128_desc(sb + kX + ks * 2048, 8192, 1024), kIdescWU, ks > 0);
-                mma_f16_ss(tmem + 128, a, sw128_desc(sb + kV + ks * 2048, 8192, 1024), kIdescWU, ks > 0);
-            }
+            for (int ks = 0; ks < 4; ++ks)  // K = 16 rows per MMA
+                mma_f16_ss(tmem, sw128_desc(sb + kT16 + ks * 32, 16, 1024),
+                           sw128_desc(sb + kX + ks * 2048, 8192, 1024), kIdescWU, ks > 0);
             mma_commit(&bar[2]);
-        }
-        const bool ok_wu = !__syncthreads_or(!mbar_wait(&bar[2], n_local & 1));
-        tc_fence_after();
-        if (!ok_wu) {  // the product never completed: report and stop (uniform)
-            if (tid == 0 && p.status) atomicOr(p.status, 1);
-            break;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_f16_ss(tmem + 128, sw128_desc(sb + kT16 + ks * 32, 16, 1024),
+                           sw128_desc(sb + kV + ks * 2048, 8192, 1024), kIdescWU, ks > 0);
+            mma_commit(bar_u);
         }
 
-        // ---- w and u out of tensor memory into their staging tiles: warp w reads
-        //      lane quarter qd = w % 4, whose lanes 0..15 hold chunk rows 16 qd +
-        //      lane; part w / 4 takes 64 of the 256 columns (0, 1: w; 2, 3: u).
+        // ---- w, then u, out of tensor memory into their staging tiles: warp w
+        //      reads lane quarter qd = w % 4, whose lanes 0..15 hold chunk rows
+        //      16 qd + lane, and columns 32 cb .. 32 cb + 31 (cb = w / 4) of each.
+        //      A wait that gives up is reported at the barrier that closes the
+        //      read-back (the values read are then not stored).
+        bool ok_wu = true;
         {
-            const int qd = warp & 3, part = warp >> 2;
+            const int qd = warp & 3, cb = warp >> 2;
             const int i = 16 * qd + (lane & 15);
-            const uint32_t tcol = tmem + ((uint32_t)(32 * qd) << 16) + 64 * part;
-            float x[4][16];  // the part's 64 columns, loaded before one wait
+            const uint32_t tcol = tmem + ((uint32_t)(32 * qd) << 16) + 32 * cb;
 #pragma unroll
-            for (int h = 0; h < 4; ++h) tmem_ld16(tcol + 16 * h, x[h]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int m = 0; m < 2; ++m) {  // 0: w, 1: u
+                ok_wu = mbar_wait(m == 0 ? &bar[2] : bar_u, n_local & 1) && ok_wu;
+                tc_fence_after();
+                float x[2][16];
+                tmem_ld16(tcol + 128 * m, x[0]);
+                tmem_ld16(tcol + 128 * m + 16, x[1]);
+                tmem_wait_ld();
                 if (lane < 16) {
 #pragma unroll
                     for (int g2 = 0; g2 < 2; ++g2) {
-                        const float* xv = x[2 * h + g2];
+                        const float* xv = x[g2];
                         const uint4 lo = make_uint4(pack_half2(xv[0], xv[1]), pack_half2(xv[2], xv[3]),
                                                     pack_half2(xv[4], xv[5]), pack_half2(xv[6], xv[7]));
                         const uint4 hi = make_uint4(pack_half2(xv[8], xv[9]), pack_half2(xv[10], xv[11]),
                                                     pack_half2(xv[12], xv[13]), pack_half2(xv[14], xv[15]));
-                        const int c16 = 32 * h + 16 * g2;  // column within the part
-                        if (part < 2) {
-                            const int c = 64 * part + c16;
+                        const int c = 32 * cb + 16 * g2;  // column of w or u
+                        if (m == 0) {
                             *reinterpret_cast<uint4*>(smem + kLQ + sw128_off(i, c, 64)) = lo;
                             *reinterpret_cast<uint4*>(smem + kLQ + sw128_off(i, c + 8, 64)) = hi;
                         } else {
-                            const int slice = 4 * (part - 2) + (c16 >> 4);  // 16 value columns each
-                            uint8_t* dst = smem + kLq32 + slice * kWsUSliceBytes + i * 32;
+                            uint8_t* dst = smem + kLq32 + (c >> 4) * kWsUSliceBytes + i * 32;  // 16 value columns a slice
                             *reinterpret_cast<uint4*>(dst) = lo;
                             *reinterpret_cast<uint4*>(dst + 16) = hi;
                         }
@@ -764,7 +768,10 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
         }
         tc_fence_before();
         fence_proxy_async();
-        __syncthreads();
+        if (__syncthreads_or(!ok_wu)) {  // a product never completed: report and stop (uniform)
+            if (tid == 0 && p.status) atomicOr(p.status, 1);
+            break;
+        }
         if (tid == kStoreTid) {
             bulk_s2g(blk + kWsWOff, smem + kLQ, 16384);
             bulk_s2g(blk + kWsUOff, smem + kLq32, 16384);
