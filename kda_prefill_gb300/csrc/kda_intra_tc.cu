@@ -136,6 +136,7 @@ __device__ __forceinline__ void publish_ready(int* flag) {
 // Item claims of the standalone launch: item blockIdx.x, then every
 // gridDim.x-th.
 struct StaticClaims {
+    static constexpr bool kNextAtTop = false;  // next() may wait for part 1's barrier
     __device__ int first() { return blockIdx.x; }
     __device__ void claim() {}
     __device__ int next(int it) { return it + gridDim.x; }
@@ -236,6 +237,9 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBar);  // [0] q,k,g  [1] v  [2] w MMA
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kBar + 24);  // tensor-memory base
     uint64_t* bar_u = reinterpret_cast<uint64_t*>(smem + kBar + 40);  // u MMA
+    // raised before a CTA barrier by a thread whose bounded wait gave up, read by
+    // every thread after it, so that all leave the item loop together
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBar + 48);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -254,6 +258,7 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
         mbar_init(&bar[1], 1);
         mbar_init(&bar[2], 1);
         mbar_init(bar_u, 1);
+        *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&maps.q);
         prefetch_tmap(&maps.k);
@@ -341,18 +346,23 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
         const int len = len_next;
         const float braw = braw_next;
         uint8_t* blk = p.ws + (size_t)it * kWsBytes;
+        int nxt = n_items;  // the next item, read after part 1's barrier
         cl.claim();
 
+        // the inputs' wait gives up only if a copy never lands: for claims read
+        // at the item's start, the loop stops at a reduction barrier here; else
+        // part 1 works on stale data and the loop stops at part 1's barrier
         const bool ok_in = mbar_wait(&bar[0], n_local & 1);
-        if (__syncthreads_or(!ok_in)) {
-            if (tid == 0 && p.status) atomicOr(p.status, 1);
-            break;
-        }
-        const int nxt = cl.next(it);
-        // the next item's chunk metadata, loaded while this one runs
-        if (nxt < n_items) {
-            tok_next = item_tok(nxt);
-            len_next = item_len(nxt, tok_next);
+        if constexpr (Claims::kNextAtTop) {
+            if (__syncthreads_or(!ok_in)) {
+                if (tid == 0 && p.status) atomicOr(p.status, 1);
+                break;
+            }
+            nxt = cl.next(it);
+            if (nxt < n_items) {
+                tok_next = item_tok(nxt);
+                len_next = item_len(nxt, tok_next);
+            }
         }
 
         // ---- decay pass, all warps: thread (block B, row half hf, channels c0,
@@ -430,7 +440,20 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
             // part 2 rewrites them (their completion, for the fused launch's ready
             // flag, is awaited during the tiles, off the CTA's barriers)
             if (tid == kStoreTid) bulk_wait_read_all();
+            if (!Claims::kNextAtTop && !ok_in) *abort_flag = 1;
             __syncthreads();
+            if constexpr (!Claims::kNextAtTop) {
+                if (*abort_flag) {  // uniform: every thread reads the flag after the barrier
+                    if (tid == 0 && p.status) atomicOr(p.status, 1);
+                    break;
+                }
+                nxt = cl.next(it);
+                // the next item's chunk metadata, loaded while this one runs
+                if (nxt < n_items) {
+                    tok_next = item_tok(nxt);
+                    len_next = item_len(nxt, tok_next);
+                }
+            }
             {
                 // row norms: lane 2v (v = 2i + s) forms the norm factor of value v
                 // (row i, s = 0: q with 1/sqrt(K), 1: k), then all lanes take theirs
@@ -768,7 +791,15 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
         }
         tc_fence_before();
         fence_proxy_async();
-        if (__syncthreads_or(!ok_wu)) {  // a product never completed: report and stop (uniform)
+        bool stop;
+        if constexpr (Claims::kNextAtTop) {
+            stop = __syncthreads_or(!ok_wu);
+        } else {
+            if (!ok_wu) *abort_flag = 1;
+            __syncthreads();
+            stop = *abort_flag;
+        }
+        if (stop) {  // a product never completed: report and stop (uniform)
             if (tid == 0 && p.status) atomicOr(p.status, 1);
             break;
         }
@@ -814,6 +845,7 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
 // the split chosen so that the intra items stay ahead of the walks, the scan
 // runs alongside the second part of the intra work instead of after it.
 struct QueueClaims {
+    static constexpr bool kNextAtTop = true;  // a barrier at the item's start, then next()
     int* queue;
     volatile int* slot;  // the claimed position, shared memory
     int split, n_walks, n_items;
