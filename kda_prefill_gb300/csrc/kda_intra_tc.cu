@@ -136,7 +136,6 @@ __device__ __forceinline__ void publish_ready(int* flag) {
 // Item claims of the standalone launch: item blockIdx.x, then every
 // gridDim.x-th.
 struct StaticClaims {
-    static constexpr bool kNextAtTop = false;  // next() may wait for part 1's barrier
     __device__ int first() { return blockIdx.x; }
     __device__ void claim() {}
     __device__ int next(int it) { return it + gridDim.x; }
@@ -349,21 +348,9 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
         int nxt = n_items;  // the next item, read after part 1's barrier
         cl.claim();
 
-        // the inputs' wait gives up only if a copy never lands: for claims read
-        // at the item's start, the loop stops at a reduction barrier here; else
-        // part 1 works on stale data and the loop stops at part 1's barrier
+        // the inputs' wait gives up only if a copy never lands; part 1 then works
+        // on stale data and the loop stops at part 1's barrier
         const bool ok_in = mbar_wait(&bar[0], n_local & 1);
-        if constexpr (Claims::kNextAtTop) {
-            if (__syncthreads_or(!ok_in)) {
-                if (tid == 0 && p.status) atomicOr(p.status, 1);
-                break;
-            }
-            nxt = cl.next(it);
-            if (nxt < n_items) {
-                tok_next = item_tok(nxt);
-                len_next = item_len(nxt, tok_next);
-            }
-        }
 
         // ---- decay pass, all warps: thread (block B, row half hf, channels c0,
         //      c0 + 1) over 8 rows.  Part 1: a = e^{lb sigmoid(g)}, the half's
@@ -440,19 +427,18 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
             // part 2 rewrites them (their completion, for the fused launch's ready
             // flag, is awaited during the tiles, off the CTA's barriers)
             if (tid == kStoreTid) bulk_wait_read_all();
-            if (!Claims::kNextAtTop && !ok_in) *abort_flag = 1;
+            if (!ok_in) *abort_flag = 1;
             __syncthreads();
-            if constexpr (!Claims::kNextAtTop) {
-                if (*abort_flag) {  // uniform: every thread reads the flag after the barrier
-                    if (tid == 0 && p.status) atomicOr(p.status, 1);
-                    break;
-                }
-                nxt = cl.next(it);
-                // the next item's chunk metadata, loaded while this one runs
-                if (nxt < n_items) {
-                    tok_next = item_tok(nxt);
-                    len_next = item_len(nxt, tok_next);
-                }
+            if (*abort_flag) {  // uniform: every thread reads the flag after the barrier
+                if (tid == 0 && p.status) atomicOr(p.status, 1);
+                break;
+            }
+            // the claim made at the item's start is visible after the barrier
+            nxt = cl.next(it);
+            // the next item's chunk metadata, loaded while this one runs
+            if (nxt < n_items) {
+                tok_next = item_tok(nxt);
+                len_next = item_len(nxt, tok_next);
             }
             {
                 // row norms: lane 2v (v = 2i + s) forms the norm factor of value v
@@ -791,15 +777,9 @@ __device__ __forceinline__ void intra_items(const IntraMaps& maps, const FwdPara
         }
         tc_fence_before();
         fence_proxy_async();
-        bool stop;
-        if constexpr (Claims::kNextAtTop) {
-            stop = __syncthreads_or(!ok_wu);
-        } else {
-            if (!ok_wu) *abort_flag = 1;
-            __syncthreads();
-            stop = *abort_flag;
-        }
-        if (stop) {  // a product never completed: report and stop (uniform)
+        if (!ok_wu) *abort_flag = 1;
+        __syncthreads();
+        if (*abort_flag) {  // a product never completed: report and stop (uniform)
             if (tid == 0 && p.status) atomicOr(p.status, 1);
             break;
         }
@@ -845,7 +825,6 @@ kda_intra_tc(const __grid_constant__ IntraMaps maps, FwdParams p) {
 // the split chosen so that the intra items stay ahead of the walks, the scan
 // runs alongside the second part of the intra work instead of after it.
 struct QueueClaims {
-    static constexpr bool kNextAtTop = true;  // a barrier at the item's start, then next()
     int* queue;
     volatile int* slot;  // the claimed position, shared memory
     int split, n_walks, n_items;
