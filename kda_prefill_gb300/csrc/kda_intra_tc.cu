@@ -912,10 +912,10 @@ constexpr int kFusedIntraSms = 32;
 // How many intra items one SM finishes while a walk advances by one chunk (a
 // walk step takes ~0.7 us and an item ~7.3 us on GB300), and a lead of whole
 // walk steps' items done before the walks start (a CTA that claims a walk first
-// finishes its item).  Fitted on the 1 x 4096 and 1 x 16384, H = 12 prefills:
-// with the lead, 0.11 puts the split where each was fastest in a sweep of
-// 0.065 .. 0.16 without it (about 450 of 768 and 1570 of 3072 items).
-constexpr double kItemsPerWalkStep = 0.11;
+// finishes its item).  Fitted on the 1 x 4096 and 1 x 16384, H = 12 prefills
+// (sweeps of the rate, 0.065 .. 0.16, and of the lead, 3 .. 9 steps): about 430
+// of 768 and 1500 of 3072 items before the walks.
+constexpr double kItemsPerWalkStep = 0.115;
 constexpr int kWalkLeadSteps = 6;
 
 // Per device: cooperative launch supported and one fused CTA fits on an SM.
