@@ -280,6 +280,19 @@ enum kda_status_bits {
 KDA_API int kda_check_status(const void* workspace, kda_stream_t stream, int* status);
 
 /*
+ * Diagnostic of the kernels' failure path, not part of the method: enqueues on
+ * `stream` one kernel in which one thread runs the bounded wait every kernel
+ * uses on something that never happens (kind 0: an mbarrier phase nothing
+ * arrives on; kind 1: a ready flag of the fused launch that nothing sets).
+ * The wait gives up after about one second and sets KDA_STATUS_WAIT_TIMEOUT,
+ * which kda_check_status(workspace, stream, ...) then reads; nothing faults or
+ * hangs, and the context stays usable.  `workspace`: device memory of at least
+ * 256 bytes (any kda_chunk_fwd workspace), whose first 256 bytes are cleared.
+ * Returns KDA_OK, KDA_ERR_INVALID_ARG or KDA_ERR_CUDA.
+ */
+KDA_API int kda_debug_wait_timeout(int kind, void* workspace, kda_stream_t stream);
+
+/*
  * Enables (default) or disables the fused intra-chunk + scan launch for the
  * calls that follow, process-wide.  Disabled, every call runs the two kernels
  * one after the other; results are bit-identical either way (same arithmetic),

@@ -17,7 +17,7 @@ __all__ = [
     "chunk_fwd", "chunk_fwd_dense", "workspace_size", "chunk_size", "plan_chunks",
     "release_cache", "cache_entries", "load_library", "KDAError", "STATE_DTYPES",
     "set_kernel_timing", "kernel_times", "set_fused_launch", "check_status",
-    "STATUS_WAIT_TIMEOUT", "STATUS_SMEM_ALIGN", "STATUS_BAD_SLOT", "STATUS_BOUNDS_MISMATCH",
+    "debug_wait_timeout", "STATUS_WAIT_TIMEOUT", "STATUS_SMEM_ALIGN", "STATUS_BAD_SLOT", "STATUS_BOUNDS_MISMATCH",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -38,6 +38,7 @@ EXPORTED = (
     "kda_plan_chunks", "kda_last_error", "kda_release_cache", "kda_cache_entries",
     "kda_set_kernel_timing", "kda_kernel_times", "kda_kernel_name", "kda_chunk_fwd_raw_bf16",
     "kda_chunk_fwd_noalloc", "kda_set_fused_launch", "kda_check_status",
+    "kda_debug_wait_timeout",
 )
 
 
@@ -100,6 +101,8 @@ def load_library(path: str = LIB_PATH):
     lib.kda_set_fused_launch.argtypes = [ctypes.c_int]
     lib.kda_check_status.restype = ctypes.c_int
     lib.kda_check_status.argtypes = [_vp, _vp, _vp]
+    lib.kda_debug_wait_timeout.restype = ctypes.c_int
+    lib.kda_debug_wait_timeout.argtypes = [ctypes.c_int, _vp, _vp]
     lib.kda_kernel_times.restype = ctypes.c_int
     lib.kda_kernel_times.argtypes = [_vp, ctypes.c_int, _vp, _vp]
     lib.kda_kernel_name.restype = ctypes.c_char_p
@@ -159,6 +162,15 @@ def check_status(workspace: Optional[torch.Tensor] = None, stream=None) -> int:
     v = ctypes.c_int(0)
     _check(lib.kda_check_status(_ptr(workspace), s.cuda_stream, ctypes.byref(v)), lib)
     return int(v.value)
+
+
+def debug_wait_timeout(kind: int, workspace: torch.Tensor, stream=None) -> None:
+    """Enqueues the failure-path diagnostic: a bounded wait on something that
+    never happens (kind 0: an mbarrier, 1: a ready flag) gives up after about a
+    second and sets STATUS_WAIT_TIMEOUT in `workspace`'s status word."""
+    lib = load_library()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    _check(lib.kda_debug_wait_timeout(int(kind), _ptr(workspace), s.cuda_stream), lib)
 
 
 def set_fused_launch(enable: bool) -> None:

@@ -827,6 +827,19 @@ int kda_check_status(const void* workspace, kda_stream_t stream, int* status) {
     return KDA_OK;
 }
 
+int kda_debug_wait_timeout(int kind, void* workspace, kda_stream_t stream) {
+    if (kind != 0 && kind != 1) return fail(KDA_ERR_INVALID_ARG, "kind %d is not 0 or 1", kind);
+    if (!workspace) return fail(KDA_ERR_INVALID_ARG, "workspace is NULL");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the header (status word at 0, a zero flag at byte 128) is cleared first
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaError_t e = cudaMemsetAsync(ws, 0, kda::kWsHeader, s);
+    if (e == cudaSuccess)
+        e = kda::launch_wait_probe(kind, reinterpret_cast<int*>(ws), reinterpret_cast<const int*>(ws + 128), s);
+    if (e != cudaSuccess) return cuda_fail(e, "kda_debug_wait_timeout");
+    return KDA_OK;
+}
+
 int kda_set_fused_launch(int enable) {
     kda::set_fused_enabled(enable != 0);
     return KDA_OK;

@@ -72,8 +72,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Waits for the phase with the given parity to complete; gives up after a
 // bounded number of polls and returns false (the caller reports an error and
-// leaves the kernel instead of hanging).
-constexpr uint32_t kWaitLimit = 1u << 22;
+// leaves the kernel instead of hanging).  A failed poll suspends the thread for
+// ~3.8 us on GB300 (measured), so 2^18 polls give up after about a second.
+constexpr uint32_t kWaitLimit = 1u << 18;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     for (uint32_t i = 0; i < kWaitLimit; ++i)
         if (mbar_try_wait(bar, parity)) return true;

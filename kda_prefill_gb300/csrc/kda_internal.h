@@ -178,6 +178,10 @@ void set_fused_enabled(bool on);
 cudaError_t launch_fused(const FwdParams& p, cudaStream_t s);
 int num_sms();
 int scan_groups(int N, int H, int num_sms, int beside_pairs = 0);
+// One thread of one CTA runs a bounded wait that cannot complete (kind 0: an
+// mbarrier; 1: the zero ready flag at `flag`) and, when it gives up, ORs 1 into
+// *status.
+cudaError_t launch_wait_probe(int kind, int* status, const int* flag, cudaStream_t s);
 // A tensor map of `out` for a walk's TMA stores (box box_values values x 1 head
 // x box_rows rows); false when it cannot be made (the walk then stores directly).
 bool make_out_map(CUtensorMap* m, const FwdParams& p, int box_values, int box_rows);

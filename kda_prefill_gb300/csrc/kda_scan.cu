@@ -313,7 +313,28 @@ cudaError_t launch_scan_vp(const FwdParams& p, cudaStream_t s, bool pdl) {
                             pdl, p, out_map, has_out_map);
 }
 
+// Diagnostic: one thread waits, with the bounded waits every kernel uses, for
+// something that never happens (kind 0: an mbarrier phase nothing arrives on;
+// kind 1: a ready flag nothing sets), so that the give-up path, the status word
+// and the context's use afterwards can be tested without faulting or hanging.
+__global__ void kda_wait_probe(int kind, int* status, const int* flag) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        dev::mbar_init(&bar, 1);
+        dev::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    const bool ok = kind == 0 ? dev::mbar_wait(&bar, 0) : scan::wait_ready_run(flag, 1, 1) > 0;
+    if (!ok) atomicOr(status, 1);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_probe(int kind, int* status, const int* flag, cudaStream_t s) {
+    kda_wait_probe<<<1, 32, 0, s>>>(kind, status, flag);
+    return cudaGetLastError();
+}
 
 int scan_groups(int N, int H, int num_sms, int beside_pairs) {
     // 16 value rows per CTA while (sequence, head) pairs are few enough for the

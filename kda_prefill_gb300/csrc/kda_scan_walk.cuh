@@ -18,8 +18,9 @@ using namespace dev;
 // pair with the writers' release stores; the proxy fence then orders the blocks'
 // contents before this thread's later bulk copies (async proxy) of them.
 constexpr int kAhead = 8;
+constexpr uint32_t kFlagRounds = 1u << 22;  // about a second of rounds on GB300 (measured)
 __device__ __forceinline__ int wait_ready_run(const int* flags, int stride, int count) {
-    for (uint32_t i = 0; i < dev::kWaitLimit; ++i) {
+    for (uint32_t i = 0; i < kFlagRounds; ++i) {
         int v[kAhead];
 #pragma unroll
         for (int j = 0; j < kAhead; ++j) {

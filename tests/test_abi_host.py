@@ -96,6 +96,14 @@ def test_plan_chunks_rejects_bad_bounds(lib):
     assert b"decreases" in lib.kda_last_error()
 
 
+def test_debug_wait_timeout_rejects_bad_arguments(lib):
+    # checked before any CUDA call: a kind other than 0 or 1, a NULL workspace
+    assert lib.kda_debug_wait_timeout(2, 4096, None) == kda.KDA_ERR_INVALID_ARG
+    assert b"kind" in lib.kda_last_error()
+    assert lib.kda_debug_wait_timeout(0, None, None) == kda.KDA_ERR_INVALID_ARG
+    assert b"workspace" in lib.kda_last_error()
+
+
 def test_workspace_size_is_an_upper_bound(lib):
     C = kda.chunk_size()
     assert kda.workspace_size(0, 0, 12) == 0
